@@ -1,0 +1,104 @@
+"""Plant plausible mistakes in the oracle (CPU only) and check that a pin catches each.
+
+Every case swaps one oracle function for a subtly wrong version (a flipped sign,
+an off-by-one index, a dropped term, a transposed operand, truncation instead of
+round-to-nearest-even) and runs the pin that should catch it.  The pin must fail.
+"""
+import numpy as np
+import pytest
+
+import oracle.attention as attention_mod
+import oracle.e4m3 as e4m3_mod
+import oracle.rope as rope_mod
+import oracle.schemes as schemes_mod
+import tests.test_oracle_attention as t_att
+import tests.test_oracle_e4m3 as t_e4m3
+import tests.test_oracle_ring as t_ring
+import tests.test_oracle_rope as t_rope
+import tests.test_oracle_schemes as t_sch
+
+
+def _rotate_sign_flipped(x, cos, sin):
+    x = np.asarray(x, np.float32)
+    y = np.empty_like(x)
+    y[..., 0::2] = x[..., 0::2] * cos + x[..., 1::2] * sin
+    y[..., 1::2] = -x[..., 0::2] * sin + x[..., 1::2] * cos
+    return y
+
+
+def _rotate_halves(x, cos, sin):
+    # "rotate-half" pairing (i, i + d/2) instead of the interleaved (2i, 2i + 1)
+    x = np.asarray(x, np.float32)
+    h = x.shape[-1] // 2
+    y = np.empty_like(x)
+    y[..., :h] = x[..., :h] * cos - x[..., h:] * sin
+    y[..., h:] = x[..., :h] * sin + x[..., h:] * cos
+    return y
+
+
+def _freqs_off_by_one(d, theta=10000.0):
+    import math
+    return [math.pow(float(theta), -2.0 * (i + 1) / d) for i in range(d // 2)]
+
+
+def _encode_truncating(x):
+    x = np.asarray(x, np.float64)
+    a = np.abs(x)
+    _, E = np.frexp(np.where(a > 0, a, 1.0))
+    q = np.ldexp(1.0, np.maximum(E - 1, -6) - 3)
+    v = np.minimum(np.floor(a / q) * q, 448.0) * np.sign(x)
+    return _ORIG_ENCODE(v)
+
+
+def _attention_no_scale(q, k, v):
+    return _ORIG_ATT(np.asarray(q) * np.sqrt(np.asarray(q).shape[-1]), k, v)
+
+
+def _attention_transposed(q, k, v):
+    # softmax over the query axis instead of the key axis
+    q = np.asarray(q, np.float64); k = np.asarray(k, np.float64); v = np.asarray(v, np.float64)
+    T, H, d = q.shape
+    out = np.zeros((T, H, d))
+    for h in range(H):
+        s = q[:, h] @ k[:, h].T / np.sqrt(d)
+        p = np.exp(s - s.max(axis=0, keepdims=True))
+        p = p / p.sum(axis=0, keepdims=True)
+        out[:, h] = p @ v[:, h]
+    return out
+
+
+def _amax_plain(k):
+    return np.abs(np.asarray(k, np.float32)).max(axis=(0, 2)).astype(np.float32)
+
+
+_ORIG_ENCODE = e4m3_mod.encode
+_ORIG_ATT = attention_mod.attention_fp64
+
+
+class _RingOffByOne(schemes_mod.WriteTimeRing):
+    def write(self, k, v):
+        slots = super().write(k, v)
+        self.head = (self.head + 1) % self.R if self.writes % 3 == 0 else self.head
+        return slots
+
+
+CASES = [
+    ("rotation sign", [(rope_mod, "rotate", _rotate_sign_flipped)], t_rope.test_unit_vector_rotates_to_cos_sin),
+    ("rotate-half pairing", [(rope_mod, "rotate", _rotate_halves)], t_rope.test_matches_complex_multiplication),
+    ("frequency index", [(rope_mod, "freqs", _freqs_off_by_one)], t_rope.test_frequencies_closed_form),
+    ("e4m3 truncation", [(e4m3_mod, "encode", _encode_truncating)], t_e4m3.test_encode_random_float32_matches_library),
+    ("missing 1/sqrt(d)", [(t_att, "attention_fp64", _attention_no_scale)], t_att.test_scale_is_one_over_sqrt_d),
+    ("softmax axis", [(t_att, "attention_fp64", _attention_transposed)], t_att.test_rows_are_convex_combinations_and_key_order_free),
+    ("K amax not pair norm", [(t_sch, "chunk_amax_k", _amax_plain)], t_sch.test_amax_k_is_largest_pair_norm_bruteforce),
+    ("ring head drift", [(t_ring, "WriteTimeRing", _RingOffByOne)], lambda: t_ring.test_logical_order_equals_shifted_window(96, 32)),
+]
+
+
+@pytest.mark.parametrize("name,patches,pin", CASES, ids=[c[0] for c in CASES])
+def test_planted_mistake_is_caught(monkeypatch, name, patches, pin):
+    for mod, attr, fn in patches:
+        monkeypatch.setattr(mod, attr, fn)
+    rope_mod._TABLE_CACHE.clear()
+    with pytest.raises(AssertionError):
+        pin()
+    rope_mod._TABLE_CACHE.clear()

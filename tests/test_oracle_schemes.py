@@ -1,0 +1,137 @@
+"""Pins for the two oracle schemes against each other and against closed forms.
+
+The pages' central claim is that doing RoPE and FP8 once at write time, with a
+ring buffer and one delta rotation per reset, reproduces the naive per-call
+upkeep.  Before any reset that is an identity (same codes, same order); after a
+reset the delta-rotated codes must sit within one e4m3 step of a fresh
+rotation at the new positions, the step taken at the larger magnitude of the
+element's RoPE pair.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from kv_cache_gb300 import synthetic
+from oracle import e4m3, rope
+from oracle.schemes import (NaiveWindow, WriteTimeRing, chunk_amax_k, chunk_amax_v,
+                            dequantise_f64, quantise, scale_inv)
+
+
+def _chunk(role, idx, T, H, d, outliers=False):
+    return synthetic.bf16_to_f32(synthetic.chunk(role, idx, T, H, d, outliers))
+
+
+def _logical(ring, arr):
+    idx = (ring.head - ring.count + np.arange(ring.count)) % ring.R
+    return arr[:, idx]
+
+
+def _pair_ulp_diff(a_codes, b_codes):
+    """|decode(a) - decode(b)| in units of the e4m3 step at max(|b0|, |b1|) of b's pair."""
+    a = e4m3.decode(a_codes)
+    b = e4m3.decode(b_codes)
+    mag = np.maximum(np.abs(b[..., 0::2]), np.abs(b[..., 1::2]))
+    mag = np.repeat(mag, 2, axis=-1)
+    return np.abs(a - b) / e4m3.ulp_at(mag)
+
+
+def test_amax_k_is_largest_pair_norm_bruteforce():
+    x = _chunk("k", 0, 5, 2, 8, outliers=True)
+    got = chunk_amax_k(x)
+    for h in range(2):
+        best = 0.0
+        for t in range(5):
+            for i in range(4):
+                best = max(best, math.hypot(float(x[t, h, 2 * i]), float(x[t, h, 2 * i + 1])))
+        assert abs(got[h] - best) <= 1e-6 * best
+    assert np.all(chunk_amax_v(x) == np.abs(x).max(axis=(0, 2)))
+
+
+def test_amax_k_rotation_invariant():
+    x = _chunk("k", 1, 64, 4, 128, outliers=True)
+    xr = rope.rotate_at(x, np.arange(30000, 30064), 128)
+    assert np.allclose(chunk_amax_k(xr), chunk_amax_k(x), rtol=1e-6, atol=0)
+
+
+def test_quantise_error_within_half_step():
+    x = _chunk("v", 2, 32, 2, 64, outliers=True)
+    amax = chunk_amax_v(x)
+    scale, inv = scale_inv(amax)
+    codes = quantise(x, inv[None, :, None])
+    back = dequantise_f64(codes, scale[None, :, None])
+    y = x.astype(np.float64) * inv[None, :, None].astype(np.float64)   # value in code units
+    err = np.abs(back / scale[None, :, None] - y)
+    assert np.all(err <= 0.5 * e4m3.ulp_at(np.abs(y)) * (1 + 1e-6) + 1e-12)
+    # the largest element maps to (almost) 448 and nothing saturates beyond it
+    assert np.max(e4m3.decode(codes)) <= 448.0 and np.max(np.abs(e4m3.decode(codes))) >= 416.0
+
+
+def test_scale_inv_zero_amax():
+    s, i = scale_inv(np.array([0.0, 448.0, 3.5], np.float32))
+    assert s[0] == 1 and i[0] == 1 and s[1] == 1 and i[1] == 1
+    assert s[2] == np.float32(3.5) / np.float32(448) and i[2] == np.float32(448) / np.float32(3.5)
+
+
+@pytest.mark.parametrize("R,T,H,d", [(96, 32, 2, 64), (100, 32, 2, 64), (37, 8, 1, 16)])
+def test_writetime_equals_naive_before_reset(R, T, H, d):
+    naive = NaiveWindow(R, H, d)
+    ring = WriteTimeRing(R, H, d)
+    for w in range(2 * R // T + 3):
+        k = _chunk("k", w, T, H, d, outliers=True)
+        v = _chunk("v", w, T, H, d, outliers=True)
+        naive.write(k, v)
+        ring.write(k, v)
+        k8, v8, ks, vs = naive.cache_codes()
+        assert np.array_equal(_logical(ring, ring.k8), k8.transpose(1, 0, 2))
+        assert np.array_equal(_logical(ring, ring.v8), v8.transpose(1, 0, 2))
+        if w % 3 == 0:
+            q = _chunk("q", w, T, H, d)
+            a = naive.attend(q)
+            b = ring.attend(q)
+            assert np.max(np.abs(a - b)) < 1e-12
+
+
+@pytest.mark.parametrize("R,T,H,d", [(96, 32, 2, 64), (100, 32, 2, 64)])
+def test_rebase_within_one_pair_step_of_fresh_rotation(R, T, H, d):
+    naive = NaiveWindow(R, H, d)
+    ring = WriteTimeRing(R, H, d)
+    worst = 0.0
+    for s in range(100):
+        if s > 0 and s % 42 == 0:
+            v_before = ring.v8.copy()
+            k_before = ring.k8.copy()
+            assert ring.rebase() == naive.rebase()
+            assert np.array_equal(ring.v8, v_before)          # V untouched
+            assert np.mean(ring.k8 != k_before) > 0.5          # K really rotated
+            k8, v8, _, _ = naive.cache_codes()
+            diff = _pair_ulp_diff(_logical(ring, ring.k8), k8.transpose(1, 0, 2))
+            worst = max(worst, float(diff.max()))
+            assert np.array_equal(_logical(ring, ring.v8), v8.transpose(1, 0, 2))
+        k = _chunk("k", s, T, H, d, outliers=True)
+        v = _chunk("v", s, T, H, d, outliers=True)
+        naive.write(k, v)
+        ring.write(k, v)
+    # one step of the pair's larger element; measured by the element's own step
+    # the worst case is hundreds of steps, since the rotation moves the large
+    # partner's rounding error into the small one
+    assert worst == 1.0
+
+
+def test_rebase_after_partial_fill_and_twice():
+    R, T, H, d = 64, 10, 1, 16
+    ring = WriteTimeRing(R, H, d)
+    naive = NaiveWindow(R, H, d)
+    for w in range(3):                    # count = 30 < R
+        k = _chunk("k", 50 + w, T, H, d)
+        ring.write(k, k); naive.write(k, k)
+    assert ring.rebase() == 0             # next_pos == count: nothing to rotate
+    assert ring.next_pos == 30
+    for w in range(9):
+        k = _chunk("k", 60 + w, T, H, d)
+        ring.write(k, k); naive.write(k, k)
+    naive.rebase(); naive.rebase()
+    d1 = ring.rebase(); d2 = ring.rebase()
+    assert d1 == 120 - 64 and d2 == 0
+    k8, _, _, _ = naive.cache_codes()
+    assert _pair_ulp_diff(_logical(ring, ring.k8), k8.transpose(1, 0, 2)).max() <= 1.0
