@@ -1,0 +1,161 @@
+/*
+ * kvring.h -- C ABI of the GB300 write-time KV cache for streaming video DiT attention.
+ *
+ * The operations follow three public reports of Runway's real-time "Characters"
+ * serving work:
+ *   [ai.info]     "Characters funziona in tempo reale su quattro H100, afferma Runway",
+ *                 sections "La gestione della cache spostata al momento della scrittura"
+ *                 and "Latenza dei turni e altre configurazioni GPU";
+ *   [neurocartel] "Runway Characters realtime on 4 H100" (neurocartel.com),
+ *                 section "Кэш: 240 attention calls и работа на запись";
+ *   [wechild]     wechild.cn news item on Runway's real-time Characters inference
+ *                 paper (untitled), paragraphs 6-8.
+ * The pages give no API; the calls below follow their statement of the problem:
+ * write once per chunk, read many times, rebase once per position reset.
+ *
+ * Conventions shared by every call
+ *   - Return value: KVRING_OK (0) or a negative KVRING_E* code.  Nothing aborts,
+ *     throws or exits across this ABI.  A call that fails a precondition leaves
+ *     the ring unchanged; the message is available from kvring_last_error().
+ *   - Device pointers are raw CUDA device addresses of the current device;
+ *     `cuda_stream` is a cudaStream_t (NULL = legacy default stream).
+ *   - Hot calls (write, attend, rebase) only enqueue work on the stream: no host
+ *     synchronisation.  The caller keeps its input/output buffers alive until the
+ *     stream reaches the call.  All calls on one ring must be ordered on a single
+ *     stream by the caller (the ring's scratch buffers are shared between calls).
+ *   - The ring owns every device buffer it allocates (FP8 K and V rings, per-slot
+ *     chunk amax, RoPE table, Q scratch, split partials, error word).  The caller
+ *     owns every buffer it passes in.
+ *   - Layouts: token-major bf16 [n][H][d] for K, V, Q inputs; fp32 [n][H][d] for
+ *     the attention output.  All element counts are in elements, not bytes.
+ */
+#ifndef KVRING_H
+#define KVRING_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------------- */
+#define KVRING_OK        0
+#define KVRING_EINVAL   (-1)  /* an argument is out of range or a pointer is NULL          */
+#define KVRING_ENOMEM   (-2)  /* a host or device allocation failed                          */
+#define KVRING_ECUDA    (-3)  /* a CUDA runtime/driver call failed (message has the reason)  */
+#define KVRING_ESTATE   (-4)  /* not valid now: attend before any write, n_q differs from the
+                                 last write, or positions would pass max_position (rebase)  */
+#define KVRING_ETIMEOUT (-5)  /* a bounded device-side wait ran out (see kvring_check_device) */
+#define KVRING_ENODEV   (-6)  /* no sm_103 device is current                                 */
+
+/* ---- configuration flags ----------------------------------------------------- */
+/* Bookkeeping only: no device memory, no CUDA calls, data pointers may be NULL.
+ * write/rebase update the host state exactly as a device ring would; attend and
+ * snapshot return KVRING_EINVAL.  Used to validate schedules on hosts without a GPU. */
+#define KVRING_FLAG_HOST_ONLY 0x1u
+
+#define KVRING_MAX_LAYERS 256
+
+typedef struct kvring kvring_t;       /* opaque */
+
+typedef struct {
+    int32_t  num_layers;             /* transformer blocks, each with its own ring: 1..256   */
+    int32_t  num_heads;              /* H: 1..256                                            */
+    int32_t  head_dim;               /* d: 64 or 128                                         */
+    int32_t  capacity;               /* R: slots per ring, 1..1048576                        */
+    int32_t  max_tokens_per_write;   /* T_max: 1..capacity                                   */
+    int32_t  max_position;           /* positions must stay below this; 0 -> 65536.  Sets the
+                                        size of the RoPE table (max_position x d/2 x 8 bytes) */
+    float    rope_theta;             /* RoPE base; 0 -> 10000                                */
+    uint32_t flags;                  /* KVRING_FLAG_*                                        */
+} kvring_config;
+
+typedef struct {
+    int64_t head;               /* next slot to write                                   */
+    int64_t count;              /* valid slots: slots [0, count) hold data              */
+    int64_t next_pos;           /* position of the next written token                   */
+    int64_t writes;             /* chunks written to this layer (the next chunk's id)   */
+    int64_t resets;             /* rebases applied (ring-wide)                          */
+    int64_t last_write_pos;     /* position of the first token of the latest chunk      */
+    int64_t last_write_tokens;  /* size of the latest chunk (0 before any write)        */
+} kvring_state;
+
+/* Create a ring set of cfg->num_layers rings.  Allocates all device memory on the
+ * current device and builds the RoPE table on the host (angles p*w_i formed and
+ * evaluated in float64, rounded once to float32; w_i = theta^(-2i/d)).
+ * Slots start empty and zeroed.  *out receives the handle (NULL on failure).
+ * Errors: EINVAL (bad config), ENODEV, ENOMEM, ECUDA. */
+int kvring_create(const kvring_config* cfg, kvring_t** out);
+
+/* Free every buffer the ring owns.  The caller makes sure no stream still uses it.
+ * NULL is accepted and ignored. */
+int kvring_destroy(kvring_t* ring);
+
+/* Write one chunk of n_tokens new tokens into layer `layer`'s ring
+ * ([ai.info] "La gestione della cache..."; [neurocartel] "Кэш...").
+ *   k_bf16, v_bf16: device, bf16 [n_tokens][H][d], token-major, contiguous.
+ * Token j goes to slot (head + j) mod R at position next_pos + j; the oldest slots
+ * are overwritten, nothing is copied.  K is rotated by RoPE at its position and
+ * both K and V are quantised to FP8 e4m3 with one scale per (head, chunk):
+ * K amax = the largest RoPE-pair norm of the chunk, V amax = the largest |v|;
+ * code = e4m3_rne_satfinite(x * (448/amax)).  The chunk's amax is stored with
+ * each of its slots and never changes.
+ * Then head += n (mod R), count = min(count + n, R), next_pos += n.
+ * n_tokens == 0 is a no-op.  Errors: EINVAL (layer, pointers, n_tokens >
+ * max_tokens_per_write), ESTATE (next_pos + n_tokens > max_position), ECUDA. */
+int kvring_write(kvring_t* ring, int32_t layer, const void* k_bf16, const void* v_bf16,
+                 int32_t n_tokens, void* cuda_stream);
+
+/* Attention of the latest chunk's queries over the finished FP8 cache of `layer`
+ * ([wechild] paragraph 6; [ai.info] "Latenza dei turni...": FP8 attention that
+ * accepts per-head scales).
+ *   q_bf16:  device, bf16 [n_q][H][d]; query i sits at position last_write_pos + i.
+ *   out_f32: device, fp32 [n_q][H][d].
+ * Q is rotated at its positions and quantised to e4m3 per (token, head) row.
+ * O = softmax(Q K^T / sqrt(d)) V over the valid slots, non-causal, every scale
+ * applied per slot.  n_q must equal the latest write's n_tokens (0 is a no-op).
+ * Errors: EINVAL, ESTATE (no write yet, n_q mismatch), ECUDA. */
+int kvring_attend(kvring_t* ring, int32_t layer, const void* q_bf16, int32_t n_q,
+                  float* out_f32, void* cuda_stream);
+
+/* Position reset of every layer ([ai.info] "La gestione della cache...": positions
+ * reset every 42 steps, one delta rotation of the cached window per reset).
+ * For each layer delta = next_pos - count; every cached K is de-quantised,
+ * rotated by -delta and re-quantised with its slot's frozen scale, in place;
+ * V is untouched; positions drop by delta and next_pos = count.  Layers with
+ * delta == 0 are skipped.  Errors: EINVAL, ECUDA. */
+int kvring_rebase(kvring_t* ring, void* cuda_stream);
+
+/* Host copy of one layer's bookkeeping (no device access).  Errors: EINVAL. */
+int kvring_get_state(const kvring_t* ring, int32_t layer, kvring_state* out);
+
+/* Synchronous copy of one layer's cache to caller-owned host buffers (tests, debug).
+ *   host_k, host_v:         uint8 [H][R][d] e4m3 codes (either may be NULL)
+ *   host_kamax, host_vamax: fp32  [H][R] chunk amax of each slot (either may be NULL)
+ *   host_pos, host_chunk:   int32 [R] position / chunk id of each slot, -1 if empty
+ * Enqueues the copies on cuda_stream and synchronises it.  Errors: EINVAL, ECUDA. */
+int kvring_snapshot(const kvring_t* ring, int32_t layer, uint8_t* host_k, uint8_t* host_v,
+                    float* host_kamax, float* host_vamax, int32_t* host_pos,
+                    int32_t* host_chunk, void* cuda_stream);
+
+/* Synchronise cuda_stream and read the ring's device error word, which kernels set
+ * when a bounded wait runs out.  Returns KVRING_OK or KVRING_ETIMEOUT (and clears
+ * the word; the message says which kernel and wait).  Errors: EINVAL, ECUDA. */
+int kvring_check_device(kvring_t* ring, void* cuda_stream);
+
+/* Message of the last failed call on this ring (or of the last failed
+ * kvring_create when ring is NULL).  Never NULL; valid until the next call. */
+const char* kvring_last_error(const kvring_t* ring);
+
+/* Testing aid for the bounded waits: make the next kvring_attend skip the K/V
+ * load of tile `skip_tile` (-1 = off) and give each device wait timeout_ns
+ * nanoseconds (0 = default of 2 s).  The skipped load makes its consumer's wait
+ * run out; the kernel then records KVRING_ETIMEOUT, waits (bounded) for its own
+ * copies in flight, frees its tensor memory and returns.  Errors: EINVAL. */
+int kvring_debug_fault(kvring_t* ring, int32_t skip_tile, int64_t timeout_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVRING_H */

@@ -1,0 +1,80 @@
+// K2: position-reset rebase -- one delta rotation of every cached K, in place.
+//
+// The pages reset positions every 42 steps and, at each reset, apply a single
+// delta rotation to the cached window instead of recomputing it (ai.info,
+// "Characters funziona in tempo reale su quattro H100", section "La gestione della
+// cache spostata al momento della scrittura"; neurocartel.com, "Runway Characters
+// realtime on 4 H100", section "Кэш: 240 attention calls и работа на запись").
+//
+// Each code is de-quantised with its slot's frozen scale, the pair is rotated by
+// -delta (cos(delta*w_i), -sin(delta*w_i), read from the RoPE table row `delta`)
+// and re-quantised with the same scale.  V has no RoPE and is not touched.
+// One launch covers every layer: a block takes one (layer, head, 128-slot block)
+// unit at a time; units of layers with delta == 0 and slots past the layer's
+// count are skipped.  16-byte loads and stores, HBM-bound.
+#include "common.cuh"
+#include "kvring_internal.h"
+
+namespace kvring_impl {
+
+constexpr int kRebaseThreads = 256;
+
+__global__ void __launch_bounds__(kRebaseThreads) rebase_kernel(const __grid_constant__ RebaseParams p) {
+    __shared__ float2 s_cs[64];
+    const int d = p.d;
+    const int c16n = d / 16;
+    const int nsb = p.Rpad / 128;
+    const long long units = (long long)p.L * p.H * nsb;
+    const int tid = threadIdx.x;
+    for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+        const int lh = (int)(u / nsb);
+        const int sb = (int)(u - (long long)lh * nsb);
+        const int l = lh / p.H;
+        const int delta = p.delta[l];
+        const int cnt = p.count[l];
+        if (delta == 0 || sb * 128 >= cnt) continue;     // uniform over the block
+        __syncthreads();                                   // previous unit done with s_cs
+        if (tid < d / 2) {
+            const float2 cs = p.rope[(size_t)delta * (d / 2) + tid];
+            s_cs[tid] = make_float2(cs.x, -cs.y);          // rotation by -delta
+        }
+        __syncthreads();
+        const int nslots = min(128, cnt - sb * 128);
+        uint8_t* base = p.k8 + ((size_t)lh * p.Rpad + (size_t)sb * 128) * d;
+        const float* am = p.kamax + (size_t)lh * p.Rpad + (size_t)sb * 128;
+#pragma unroll 2
+        for (int q = tid; q < nslots * c16n; q += kRebaseThreads) {
+            const int r = q / c16n, c = q - r * c16n;
+            uint4* ptr = reinterpret_cast<uint4*>(base + (size_t)r * d + c * 16);
+            const uint4 w = *ptr;
+            const float amax = __ldg(am + r);
+            const float sc = scale_of(amax), iv = inv_of(amax);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            uint32_t out[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f0 = e4m3x2_to_float2(ws[e] & 0xFFFFu);
+                const float2 f1 = e4m3x2_to_float2(ws[e] >> 16);
+                const float2 c0 = s_cs[c * 8 + 2 * e];
+                const float2 c1 = s_cs[c * 8 + 2 * e + 1];
+                float y0, y1, z0, z1;
+                rope_pair(__fmul_rn(f0.x, sc), __fmul_rn(f0.y, sc), c0.x, c0.y, y0, y1);
+                rope_pair(__fmul_rn(f1.x, sc), __fmul_rn(f1.y, sc), c1.x, c1.y, z0, z1);
+                out[e] = e4m3x2(__fmul_rn(y0, iv), __fmul_rn(y1, iv)) |
+                         (e4m3x2(__fmul_rn(z0, iv), __fmul_rn(z1, iv)) << 16);
+            }
+            *ptr = make_uint4(out[0], out[1], out[2], out[3]);
+        }
+    }
+}
+
+cudaError_t launch_rebase(const RebaseParams& p, int num_sms, cudaStream_t s) {
+    const long long units = (long long)p.L * p.H * (p.Rpad / 128);
+    long long grid = (long long)num_sms * 8;
+    if (grid > units) grid = units;
+    if (grid < 1) grid = 1;
+    rebase_kernel<<<(unsigned)grid, kRebaseThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace kvring_impl

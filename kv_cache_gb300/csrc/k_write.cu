@@ -1,0 +1,179 @@
+// K1: write one chunk into a layer's ring -- RoPE on K, per-(head, chunk) amax,
+// FP8 e4m3 quantisation, store into the ring slots.  One pass over the input.
+//
+// The pages move RoPE and FP8 quantisation to the moment a chunk enters the cache
+// and keep the cache as a ring buffer, so nothing is copied as the window advances
+// (ai.info, "Characters funziona in tempo reale su quattro H100", section "La
+// gestione della cache spostata al momento della scrittura"; neurocartel.com,
+// "Runway Characters realtime on 4 H100", section "Кэш: 240 attention calls и
+// работа на запись").
+//
+// Launch: grid (CL, H, 2), one thread-block cluster of CL <= 8 CTAs per (head,
+// K|V).  The chunk's slots are cut into 16-slot groups aligned in the ring
+// (the V ring is slot-contiguous, so a group is one 16-byte store per head_dim
+// row); the groups are dealt to the cluster's CTAs in ring order.  Each CTA
+// stages its rows in shared memory, takes its local amax, the cluster reduces
+// the amax through distributed shared memory, and each CTA quantises its rows
+// from shared memory.  Input bytes are read once.
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+#include "kvring_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace kvring_impl {
+
+constexpr int kWriteThreads = 256;
+
+// Token written to the j-th slot of visit-order group k of this chunk, or -1.
+__device__ __forceinline__ int group_slot_token(const WriteParams& p, int k, int j, int& slot) {
+    int g = p.group0 + k;
+    if (g >= p.ngroups_ring) g -= p.ngroups_ring;
+    const int s = g * 16 + j;
+    slot = s;
+    if (s >= p.R) return -1;
+    int t = s - (int)p.head;
+    if (t < 0) t += p.R;
+    return t < p.T ? t : -1;
+}
+
+__global__ void __launch_bounds__(kWriteThreads) write_kernel(const __grid_constant__ WriteParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ float s_red[kWriteThreads / 32];
+    __shared__ float s_amax;
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int CL = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    const int h = blockIdx.y;
+    const bool is_v = blockIdx.z == 1;
+    const int d = p.d;
+    const int tid = threadIdx.x;
+    const int k0 = rank * p.groups / CL;
+    const int k1 = (rank + 1) * p.groups / CL;
+    const int nloc = (k1 - k0) * 16;
+    uint16_t* sx = reinterpret_cast<uint16_t*>(smem);     // [nloc][d] bf16
+
+    // ---- 1. stage rows, local amax (K: largest pair norm of the un-rotated pairs; V: largest |v|)
+    const uint16_t* src = is_v ? p.v : p.k;
+    const int vec_per_row = d / 8;
+    float local = 0.f;
+#pragma unroll 4
+    for (int q = tid; q < nloc * vec_per_row; q += kWriteThreads) {
+        const int li = q / vec_per_row, c = q - li * vec_per_row;
+        int slot;
+        const int t = group_slot_token(p, k0 + li / 16, li % 16, slot);
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (t >= 0) {
+            w = __ldg(reinterpret_cast<const uint4*>(src + ((size_t)t * p.H + h) * d + c * 8));
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float x0 = bf16_lo(ws[e]), x1 = bf16_hi(ws[e]);
+                local = is_v ? fmaxf(local, fmaxf(fabsf(x0), fabsf(x1))) : fmaxf(local, pair_norm(x0, x1));
+            }
+        }
+        *reinterpret_cast<uint4*>(sx + (size_t)li * d + c * 8) = w;
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) local = fmaxf(local, __shfl_xor_sync(0xffffffffu, local, off));
+    if ((tid & 31) == 0) s_red[tid >> 5] = local;
+    __syncthreads();
+    if (tid == 0) {
+        float m = 0.f;
+        for (int w = 0; w < kWriteThreads / 32; ++w) m = fmaxf(m, s_red[w]);
+        s_amax = m;
+    }
+    // ---- 2. chunk amax over the cluster (distributed shared memory)
+    cluster.sync();
+    float amax = 0.f;
+    for (int r = 0; r < CL; ++r) amax = fmaxf(amax, *cluster.map_shared_rank(&s_amax, r));
+    const float inv = inv_of(amax);
+
+    // ---- 3. quantise and store
+    if (!is_v) {
+        const int c16n = d / 16;
+        for (int q = tid; q < nloc * c16n; q += kWriteThreads) {
+            const int li = q / c16n, c = q - li * c16n;
+            int slot;
+            const int t = group_slot_token(p, k0 + li / 16, li % 16, slot);
+            if (t < 0) continue;
+            const uint4* xs = reinterpret_cast<const uint4*>(sx + (size_t)li * d + c * 16);
+            const uint4 a = xs[0], b = xs[1];
+            const uint32_t ws[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            const float4* tab = reinterpret_cast<const float4*>(p.rope + (size_t)(p.pos0 + t) * (d / 2) + c * 8);
+            uint32_t out[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+                const float4 cs = __ldg(tab + e2);          // pairs 2*e2 and 2*e2+1
+                float y0, y1, z0, z1;
+                rope_pair(bf16_lo(ws[2 * e2]), bf16_hi(ws[2 * e2]), cs.x, cs.y, y0, y1);
+                rope_pair(bf16_lo(ws[2 * e2 + 1]), bf16_hi(ws[2 * e2 + 1]), cs.z, cs.w, z0, z1);
+                out[e2] = e4m3x2(__fmul_rn(y0, inv), __fmul_rn(y1, inv)) |
+                          (e4m3x2(__fmul_rn(z0, inv), __fmul_rn(z1, inv)) << 16);
+            }
+            *reinterpret_cast<uint4*>(p.k8 + ((size_t)h * p.Rpad + slot) * d + c * 16) =
+                make_uint4(out[0], out[1], out[2], out[3]);
+        }
+    } else {
+        const int ng = k1 - k0;
+        for (int q = tid; q < d * ng; q += kWriteThreads) {
+            const int kk = q / d, dd = q - kk * d;
+            uint32_t words[4] = {0u, 0u, 0u, 0u};
+            uint32_t written = 0;    // bit j: slot j of the group belongs to this chunk
+            int slot0 = 0;
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+                int s0, s1;
+                const int t0 = group_slot_token(p, k0 + kk, j, s0);
+                const int t1 = group_slot_token(p, k0 + kk, j + 1, s1);
+                if (j == 0) slot0 = s0;
+                const float v0 = t0 >= 0 ? bf16_lo(sx[(size_t)(kk * 16 + j) * d + dd]) : 0.f;
+                const float v1 = t1 >= 0 ? bf16_lo(sx[(size_t)(kk * 16 + j + 1) * d + dd]) : 0.f;
+                const uint32_t two = e4m3x2(__fmul_rn(v0, inv), __fmul_rn(v1, inv));
+                words[j / 4] |= two << (8 * (j % 4));
+                written |= (t0 >= 0 ? 1u : 0u) << j;
+                written |= (t1 >= 0 ? 1u : 0u) << (j + 1);
+            }
+            uint8_t* dst = p.vt8 + ((size_t)h * d + dd) * p.Rpad + slot0;
+            if (written == 0xFFFFu) {
+                *reinterpret_cast<uint4*>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
+            } else {
+                for (int j = 0; j < 16; ++j)
+                    if (written & (1u << j)) dst[j] = (uint8_t)(words[j / 4] >> (8 * (j % 4)));
+            }
+        }
+    }
+    float* am = is_v ? p.vamax : p.kamax;
+    for (int li = tid; li < nloc; li += kWriteThreads) {
+        int slot;
+        const int t = group_slot_token(p, k0 + li / 16, li % 16, slot);
+        if (t >= 0) am[(size_t)h * p.Rpad + slot] = amax;
+    }
+    // peers may still be reading s_amax
+    cluster.sync();
+}
+
+cudaError_t launch_write(const WriteParams& p, cudaStream_t s) {
+    const int CL = p.groups < 8 ? p.groups : 8;
+    const int per = (p.groups + CL - 1) / CL;
+    const size_t smem = (size_t)per * 16 * p.d * sizeof(uint16_t);
+    cudaError_t e = cudaFuncSetAttribute(write_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(CL, p.H, 2);
+    cfg.blockDim = dim3(kWriteThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, write_kernel, p);
+}
+
+}  // namespace kvring_impl

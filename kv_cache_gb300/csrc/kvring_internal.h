@@ -1,0 +1,97 @@
+// Internal declarations shared by the host API and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda.h>
+#include <stdint.h>
+
+#include "../../include/kvring.h"
+
+namespace kvring_impl {
+
+constexpr int kTile = 128;          // slots per KV tile, query rows per Q tile
+constexpr float kE4M3Max = 448.0f;
+
+// Device error word: [0] = status (0 or KVRING_ETIMEOUT), [1] = kernel id,
+// [2] = wait site, [3] = block index that gave up.
+enum KernelId : int { kKernelAttend = 1 };
+
+// ---------------------------------------------------------------- write (K1)
+struct WriteParams {
+    const uint16_t* k;        // bf16 [T][H][d]
+    const uint16_t* v;        // bf16 [T][H][d]
+    uint8_t* k8;              // this layer's K ring  [H][Rpad][d]
+    uint8_t* vt8;             // this layer's V ring  [H][d][Rpad] (slot-contiguous)
+    float* kamax;             // [H][Rpad]
+    float* vamax;             // [H][Rpad]
+    const float2* rope;       // [max_position][d/2] (cos, sin)
+    int64_t head;             // first slot of the chunk
+    int64_t pos0;             // position of token 0
+    int T, H, d, R, Rpad;
+    int groups;               // 16-slot groups touched by the chunk
+    int group0;               // first group in cyclic order
+    int ngroups_ring;         // ceil(R / 16)
+};
+cudaError_t launch_write(const WriteParams& p, cudaStream_t s);
+
+// ---------------------------------------------------------------- rebase (K2)
+struct RebaseParams {
+    uint8_t* k8;              // all layers [L][H][Rpad][d]
+    const float* kamax;       // all layers [L][H][Rpad]
+    const float2* rope;       // [max_position][d/2]
+    int L, H, d, Rpad;
+    int delta[KVRING_MAX_LAYERS];   // per layer; 0 = skip
+    int count[KVRING_MAX_LAYERS];   // valid slots per layer
+};
+cudaError_t launch_rebase(const RebaseParams& p, int num_sms, cudaStream_t s);
+
+// ---------------------------------------------------------------- Q prep (K3)
+struct QPrepParams {
+    const uint16_t* q;        // bf16 [T][H][d]
+    uint8_t* q8;              // [H][Tpad][d]
+    float* qamax;             // [H][Tpad]
+    const float2* rope;
+    int64_t pos0;
+    int T, Tpad, H, d;
+    int Tstride;              // row stride of q8 in rows (= Tpad_max)
+};
+cudaError_t launch_qprep(const QPrepParams& p, cudaStream_t s);
+
+// ---------------------------------------------------------------- attention (K4 + K5)
+struct AttendParams {
+    const float* kamax;       // this layer [H][Rpad]
+    const float* vamax;       // this layer [H][Rpad]
+    const float* qamax;       // [H][Tstride]
+    float* out;               // fp32 [T][H][d]          (splits == 1)
+    float* part_o;            // fp32 [splits][H][Tstride][d]   (splits > 1)
+    float* part_ml;           // fp32 [splits][H][Tstride][2]
+    int* err;                 // device error word
+    int T, H, d, Rpad, Tstride;
+    int count;                // valid slots
+    int layer;
+    int qtiles;               // ceil(T / 128)
+    int splits;               // KV splits per (head, q tile)
+    int tiles_per_split;
+    int ntiles;               // ceil(count / 128)
+    float log2e_rsqrt_d;      // log2(e) / sqrt(d)
+    long long timeout_ns;
+    int skip_tile;            // testing aid: K/V load of this tile is not issued (-1 = off)
+};
+struct AttendMaps {
+    CUtensorMap q8;           // 3-D {d, Tstride, H}
+    CUtensorMap k8;           // 3-D {d, Rpad, L*H}
+    CUtensorMap vt8;          // 3-D {Rpad, d, L*H}
+};
+cudaError_t launch_attend(const AttendParams& p, const AttendMaps& maps, cudaStream_t s);
+
+struct CombineParams {
+    const float* part_o;
+    const float* part_ml;
+    float* out;
+    int T, H, d, Tstride, splits;
+};
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
+
+size_t attend_smem_bytes(int d);
+
+}  // namespace kvring_impl

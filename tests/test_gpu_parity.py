@@ -1,0 +1,185 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the same seeded inputs.
+
+Bars: ring indices, positions and chunk ids bit-exact; FP8 K/V codes identical on
+>= 99.9% of elements and never more than one e4m3 step apart; chunk amax exact;
+attention max-abs <= 2e-2 and mean relative error <= 5e-3 against the oracle's
+float64 attention over its own (identical) dequantised cache.
+"""
+import numpy as np
+import pytest
+
+from kv_cache_gb300 import kvring as kv
+from oracle.schemes import WriteTimeRing
+from tests._lib import ensure_built
+from tests.gpu_util import (assert_attention_close, assert_codes_match, chunk_pair, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_built()
+
+
+def _check_cache(ring, layer, o: WriteTimeRing, min_identical=0.999):
+    snap = ring.snapshot(layer)
+    st = ring.state(layer)
+    assert (st["head"], st["count"], st["next_pos"], st["writes"]) == (o.head, o.count, o.next_pos, o.writes)
+    assert np.array_equal(snap["pos"].astype(np.int64), o.pos)
+    assert np.array_equal(snap["chunk"].astype(np.int64), o.chunk)
+    valid = o.pos >= 0
+    assert np.array_equal(snap["kamax"][:, valid], o.kamax[:, valid])
+    assert np.array_equal(snap["vamax"][:, valid], o.vamax[:, valid])
+    fk = assert_codes_match(snap["k"][:, valid], o.k8[:, valid], min_identical, "K codes")
+    fv = assert_codes_match(snap["v"][:, valid], o.v8[:, valid], min_identical, "V codes")
+    return fk, fv
+
+
+@pytest.mark.parametrize("R,T,H,d,outliers", [(96, 32, 2, 64, False), (100, 32, 2, 64, True),
+                                               (300, 100, 3, 128, True), (16, 16, 1, 128, False)])
+def test_write_small(R, T, H, d, outliers):
+    ring = kv.KVRing(1, H, d, R, T, max_position=4096)
+    o = WriteTimeRing(R, H, d)
+    for w in range(2 * R // T + 3):
+        kb, kf = chunk_pair("k", w, T, H, d, outliers)
+        vb, vf = chunk_pair("v", w, T, H, d, outliers)
+        ring.write(0, to_dev(kb), to_dev(vb))
+        o.write(kf, vf)
+        fk, fv = _check_cache(ring, 0, o)
+        assert fk == 1.0 and fv == 1.0
+
+
+def test_write_production_shape():
+    R, T, H, d = 5788, 757, 16, 128
+    ring = kv.KVRing(1, H, d, R, T, max_position=8192)
+    o = WriteTimeRing(R, H, d)
+    for w in range(9):                       # fills, then wraps (the 9th write straddles the end)
+        kb, kf = chunk_pair("k", w, T, H, d, True)
+        vb, vf = chunk_pair("v", w, T, H, d, True)
+        ring.write(0, to_dev(kb), to_dev(vb))
+        o.write(kf, vf)
+    fk, fv = _check_cache(ring, 0, o)
+    assert fk == 1.0 and fv == 1.0
+
+
+@pytest.mark.parametrize("R,T,H,d", [(96, 32, 2, 64), (100, 32, 2, 64), (300, 100, 2, 128)])
+def test_attend_small(R, T, H, d):
+    ring = kv.KVRing(1, H, d, R, T, max_position=4096)
+    o = WriteTimeRing(R, H, d)
+    for w in range(2 * R // T + 2):
+        kb, kf = chunk_pair("k", w, T, H, d, True)
+        vb, vf = chunk_pair("v", w, T, H, d, True)
+        ring.write(0, to_dev(kb), to_dev(vb))
+        o.write(kf, vf)
+        qb, qf = chunk_pair("q", w, T, H, d, True)
+        out = ring.attend(0, to_dev(qb)).cpu().numpy()
+        assert_attention_close(out, o.attend(qf), f"write {w}")
+
+
+def test_attend_warmup_partial_ring():
+    # count < R: slots past count are never written and must be masked
+    R, T, H, d = 1000, 130, 2, 128
+    ring = kv.KVRing(1, H, d, R, T)
+    o = WriteTimeRing(R, H, d)
+    for w in range(3):
+        kb, kf = chunk_pair("k", 100 + w, T, H, d)
+        vb, vf = chunk_pair("v", 100 + w, T, H, d)
+        ring.write(0, to_dev(kb), to_dev(vb))
+        o.write(kf, vf)
+        qb, qf = chunk_pair("q", 100 + w, T, H, d)
+        assert_attention_close(ring.attend(0, to_dev(qb)).cpu().numpy(), o.attend(qf))
+
+
+def test_attend_production_sampled():
+    R, T, H, d = 5788, 757, 16, 128
+    ring = kv.KVRing(1, H, d, R, T, max_position=8192)
+    o = WriteTimeRing(R, H, d)
+    for w in range(9):
+        kb, kf = chunk_pair("k", w, T, H, d, True)
+        vb, vf = chunk_pair("v", w, T, H, d, True)
+        ring.write(0, to_dev(kb), to_dev(vb))
+        o.write(kf, vf)
+    qb, qf = chunk_pair("q", 9, T, H, d, True)
+    out = ring.attend(0, to_dev(qb)).cpu().numpy()
+    rng = np.random.default_rng(7)
+    heads = np.array([0, 5, 10, 15])
+    rows = np.unique(np.concatenate([rng.choice(T, 60, replace=False), [0, 127, 128, 640, 756]]))
+    ref = o.attend(qf, heads=heads, rows=rows)
+    assert_attention_close(out[np.ix_(rows, heads)], ref, "production sample")
+
+
+def test_step_sequence_with_resets_tiny():
+    """100 steps of the tiny case: write, 4 attends, resets at 42 and 84."""
+    L, R, T, H, d = 2, 96, 32, 2, 64
+    ring = kv.KVRing(L, H, d, R, T, max_position=R + 42 * T)
+    oracles = [WriteTimeRing(R, H, d) for _ in range(L)]
+    for s in range(100):
+        if s > 0 and s % 42 == 0:
+            ring.rebase()
+            for o in oracles:
+                o.rebase()
+            for l in range(L):
+                _check_cache(ring, l, oracles[l])
+        for l in range(L):
+            kb, kf = chunk_pair("k", s * L + l, T, H, d, True)
+            vb, vf = chunk_pair("v", s * L + l, T, H, d, True)
+            ring.write(l, to_dev(kb), to_dev(vb))
+            oracles[l].write(kf, vf)
+            for p in range(4):
+                qb, qf = chunk_pair("q", (s * L + l) * 4 + p, T, H, d)
+                out = ring.attend(l, to_dev(qb))
+                if s % 7 == 0 or s in (41, 42, 43, 84, 85, 99):
+                    assert_attention_close(out.cpu().numpy(), oracles[l].attend(qf), f"step {s} layer {l}")
+        if s % 10 == 0 or s in (41, 42, 43, 83, 84, 85, 99):
+            for l in range(L):
+                _check_cache(ring, l, oracles[l])
+
+
+def test_rebase_many_layers_production_heads():
+    """Rebase over several layers at production head shape; bytes bit-exact with the oracle."""
+    L, R, T, H, d = 3, 5788, 757, 16, 128
+    ring = kv.KVRing(L, H, d, R, T, max_position=R + 42 * T)
+    oracles = [WriteTimeRing(R, H, d) for _ in range(L)]
+    for w in range(9):
+        for l in range(L):
+            kb, kf = chunk_pair("k", 10 * w + l, T, H, d, True)
+            vb, vf = chunk_pair("v", 10 * w + l, T, H, d, True)
+            ring.write(l, to_dev(kb), to_dev(vb))
+            oracles[l].write(kf, vf)
+    ring.rebase()
+    for o in oracles:
+        o.rebase()
+    for l in range(L):
+        fk, fv = _check_cache(ring, l, oracles[l])
+        assert fk == 1.0 and fv == 1.0
+
+
+def test_edge_sizes():
+    # T = 1, T = R (whole ring in one write), then a write that wraps mid-group
+    R, H, d = 40, 1, 64
+    ring = kv.KVRing(1, H, d, R, R, max_position=4096)
+    o = WriteTimeRing(R, H, d)
+    for w, T in enumerate([1, 40, 3, 17, 40, 1, 23]):
+        kb, kf = chunk_pair("k", 200 + w, T, H, d, True)
+        vb, vf = chunk_pair("v", 200 + w, T, H, d, True)
+        ring.write(0, to_dev(kb), to_dev(vb))
+        o.write(kf, vf)
+        fk, fv = _check_cache(ring, 0, o)
+        assert fk == 1.0 and fv == 1.0
+        qb, qf = chunk_pair("q", 200 + w, T, H, d)
+        assert_attention_close(ring.attend(0, to_dev(qb)).cpu().numpy(), o.attend(qf), f"T={T}")
+
+
+def test_state_errors_on_device_ring():
+    ring = kv.KVRing(1, 2, 64, 96, 32)
+    qb, _ = chunk_pair("q", 0, 32, 2, 64)
+    with pytest.raises(kv.KVRingError) as e:
+        ring.attend(0, to_dev(qb))
+    assert e.value.code == kv.KVRING_ESTATE
+    kb, _ = chunk_pair("k", 0, 32, 2, 64)
+    ring.write(0, to_dev(kb), to_dev(kb))
+    qb16, _ = chunk_pair("q", 0, 16, 2, 64)
+    with pytest.raises(kv.KVRingError) as e:
+        ring.attend(0, to_dev(qb16))
+    assert e.value.code == kv.KVRING_ESTATE
+    assert ring.check_device() == kv.KVRING_OK
