@@ -1,0 +1,355 @@
+"""Benchmark of the write-time KV-cache hot path on GB300 (one JSON line on stdout).
+
+Workload (default): the steady denoise step of a 60-block streaming video DiT --
+every block has its own 5,788-slot ring of 16 heads x 128; each step writes one
+757-token chunk per block and runs 4 attention calls per block (240 per step),
+with the position reset (one delta rotation of every cached K) every 42 steps.
+A "step" is one pass of the whole hot path: [rebase when due] + 60 x write +
+240 x attend, enqueued through the C ABI on one stream.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kvring|reference]
+
+* value: steps/s over all ranks (replicas: each rank runs the full workload on
+  its own GPU; no data-path collective), inputs resident in HBM.
+* e2e: the same steps with each step's K, V, Q copied host->device from pinned
+  memory and every attention output copied back, inside the timed region.
+* roofline: the attention call (Q-prep + attention + split combine launches),
+  algorithmic FLOP 4*T*R*d*H per call at a full ring, against the measured
+  bf16 peak x 2 (FP8); plus the write kernel against measured HBM bandwidth.
+* cpu_baseline / --impl reference: the CPU oracle (naive per-call upkeep, then
+  float64 attention) timed on this host on a bounded sample (one block's
+  write + 4 attention calls), extrapolated to a 60-block step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "cache upkeep ms/step & GB/s; FP8 attn TFLOP/s (757q×5788kv); % of GB300 roofline"
+WORKLOAD = dict(name="steady denoise step: 60 blocks x (1 write + 4 attention calls), reset every 42 steps",
+                L=60, H=16, d=128, R=5788, T=757, passes=4, reset_every=42)
+SMALL = dict(name="small check: 4 blocks x (1 write + 4 attention calls)", L=4, H=16, d=128, R=5788, T=757,
+             passes=4, reset_every=42)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        load = [x for x in sm if smax and x > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make_pool(cfg, torch, device):
+    from kv_cache_gb300 import synthetic
+    T, H, d = cfg["T"], cfg["H"], cfg["d"]
+    host = {r: [synthetic.chunk(r, i, T, H, d, outliers=True) for i in range(synthetic.POOL)] for r in ("k", "v", "q")}
+    dev = {r: [torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(device) for b in host[r]] for r in host}
+    return host, dev
+
+
+def run_gpu(args, cfg, rank, world):
+    import torch
+    from kv_cache_gb300 import kvring as kv
+    from kv_cache_gb300 import synthetic
+
+    device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(device)
+    kv.load()
+    L, H, d, R, T, P, RE = (cfg[k] for k in ("L", "H", "d", "R", "T", "passes", "reset_every"))
+    ring = kv.KVRing(L, H, d, R, T, max_position=R + RE * T)
+    host, pool = make_pool(cfg, torch, device)
+    stream = torch.cuda.current_stream(device)
+    outs = [torch.empty((T, H, d), dtype=torch.float32, device=device) for _ in range(P)]
+
+    step_counter = [0]
+
+    def one_step(timers=None, inputs=None):
+        s = step_counter[0]
+        step_counter[0] += 1
+        if s > 0 and s % RE == 0:
+            if timers is not None:
+                timers["rebase"][0].record(stream)
+            ring.rebase(stream)
+            if timers is not None:
+                timers["rebase"][1].record(stream)
+                timers["n_rebase"] += 1
+        for p in range(P):
+            for l in range(L):
+                if p == 0:
+                    i = synthetic.pool_index(s, l, 4, L)
+                    k = inputs["k"][l] if inputs else pool["k"][i]
+                    v = inputs["v"][l] if inputs else pool["v"][i]
+                    if timers is not None:
+                        ev = timers["write"][timers["nw"]]
+                        ev[0].record(stream)
+                    ring.write(l, k, v, stream=stream)
+                    if timers is not None:
+                        ev[1].record(stream)
+                        timers["nw"] += 1
+                q = inputs["q"][p * L + l] if inputs else pool["q"][synthetic.pool_index(s, l, p, L)]
+                if timers is not None:
+                    ev = timers["attend"][timers["na"]]
+                    ev[0].record(stream)
+                ring.attend(l, q, outs[p], stream=stream)
+                if timers is not None:
+                    ev[1].record(stream)
+                    timers["na"] += 1
+
+    # fill the rings (untimed): 8 writes reach the steady state (count = R)
+    fill = -(-R // T)
+    for _ in range(fill):
+        one_step()
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize(device)
+    ring.check_device(stream)
+
+    K = args.steps
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    timers = {"write": [(mk(), mk()) for _ in range(K * L)], "attend": [(mk(), mk()) for _ in range(K * L * P)],
+              "rebase": (mk(), mk()), "nw": 0, "na": 0, "n_rebase": 0}
+    launches0 = ring.launch_count()
+    sampler = ClockSampler(device.index)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    sampler.start()
+    t0, t1 = mk(), mk()
+    t0.record(stream)
+    for _ in range(K):
+        one_step(timers)
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    launches = ring.launch_count() - launches0
+    if ring.check_device(stream) != kv.KVRING_OK:
+        raise RuntimeError("device wait timed out during the timed region: " + kv.kvring_last_error(ring.handle))
+    ms = t0.elapsed_time(t1)
+    w_ms = [a.elapsed_time(b) for a, b in timers["write"][:timers["nw"]]]
+    a_ms = [a.elapsed_time(b) for a, b in timers["attend"][:timers["na"]]]
+    rb_ms = timers["rebase"][0].elapsed_time(timers["rebase"][1]) if timers["n_rebase"] else None
+
+    # ---- end to end: host inputs (pinned) -> device, attention outputs -> host, every step
+    e2e_steps = max(1, min(K, args.e2e_steps))
+    pin = {r: [torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).pin_memory() for b in host[r]] for r in host}
+    dev_in = {"k": [torch.empty((T, H, d), dtype=torch.bfloat16, device=device) for _ in range(L)],
+              "v": [torch.empty((T, H, d), dtype=torch.bfloat16, device=device) for _ in range(L)],
+              "q": [torch.empty((T, H, d), dtype=torch.bfloat16, device=device) for _ in range(L * P)]}
+    host_out = [torch.empty((T, H, d), dtype=torch.float32).pin_memory() for _ in range(P)]
+    h2d = d2h = 0
+    torch.cuda.synchronize(device)
+    e0, e1 = mk(), mk()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        s = step_counter[0]
+        for l in range(L):
+            i = synthetic.pool_index(s, l, 4, L)
+            dev_in["k"][l].copy_(pin["k"][i], non_blocking=True)
+            dev_in["v"][l].copy_(pin["v"][i], non_blocking=True)
+            for p in range(P):
+                dev_in["q"][p * L + l].copy_(pin["q"][synthetic.pool_index(s, l, p, L)], non_blocking=True)
+        h2d += (2 * L + P * L) * T * H * d * 2
+        one_step(inputs=dev_in)
+        for p in range(P):
+            host_out[p].copy_(outs[p], non_blocking=True)
+        d2h += P * T * H * d * 4
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = e0.elapsed_time(e1)
+    ring.close()
+    return dict(ms=ms, w_ms=w_ms, a_ms=a_ms, rb_ms=rb_ms, launches=launches, clocks=clocks,
+                e2e_ms=e2e_ms, e2e_steps=e2e_steps, h2d=h2d // e2e_steps, d2h=d2h // e2e_steps)
+
+
+def oracle_sample(cfg, seconds_hint=20.0):
+    """Time the CPU oracle on one block: a full window of writes, then one step's write + 4 calls."""
+    from kv_cache_gb300 import synthetic
+    from oracle.schemes import NaiveWindow
+
+    L, H, d, R, T, P = (cfg[k] for k in ("L", "H", "d", "R", "T", "passes"))
+    naive = NaiveWindow(R, H, d)
+    f32 = synthetic.bf16_to_f32
+    fill = -(-R // T)
+    for w in range(fill):
+        naive.write(f32(synthetic.chunk("k", w, T, H, d, True)), f32(synthetic.chunk("v", w, T, H, d, True)))
+    qs = [f32(synthetic.chunk("q", p, T, H, d, True)) for p in range(P)]
+    k = f32(synthetic.chunk("k", fill, T, H, d, True))
+    v = f32(synthetic.chunk("v", fill, T, H, d, True))
+    t0 = time.perf_counter()
+    naive.write(k, v)
+    for p in range(P):
+        naive.attend(qs[p])
+    block_s = time.perf_counter() - t0
+    step_s = block_s * L
+    threads = os.cpu_count()
+    return dict(block_s=block_s, step_s=step_s, cores=threads,
+                sample=f"one block (1 write + {P} attention calls, naive per-call upkeep, float64 attention) "
+                       f"at {H} heads x {d}, R={R}, T={T}; x{L} blocks (extrapolated)")
+
+
+def algorithmic(cfg):
+    L, H, d, R, T, P = (cfg[k] for k in ("L", "H", "d", "R", "T", "passes"))
+    write_bytes = T * H * d * 2 * 2 + T * H * d * 2           # bf16 K,V in + e4m3 K,V out
+    attend_flop = 4.0 * T * R * d * H
+    rebase_bytes = 2.0 * L * H * R * d                        # e4m3 K read + write, full rings
+    return write_bytes, attend_flop, rebase_bytes
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=42)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kvring", choices=["kvring", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=6)
+    ap.add_argument("--small", action="store_true", help="4 blocks instead of 60 (quick checks)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    cfg = SMALL if args.small else WORKLOAD
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    L, H, d, R, T, P = (cfg[k] for k in ("L", "H", "d", "R", "T", "passes"))
+    write_bytes, attend_flop, rebase_bytes = algorithmic(cfg)
+    config = {"workload": cfg["name"], "blocks": L, "heads": H, "head_dim": d, "ring_slots": R,
+              "tokens_per_write": T, "attention_calls_per_step": L * P, "reset_every_steps": cfg["reset_every"],
+              "l2": f"inputs larger than L2: {2 * L * H * R * d / 1e9:.2f} GB of e4m3 rings read per step",
+              "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        samples = [oracle_sample(cfg) for _ in range(max(1, args.steps if args.steps < 3 else 1))]
+        step_s = statistics.median(s["step_s"] for s in samples)
+        line = {"impl": "reference", "metric": METRIC, "value": 1.0 / step_s, "unit": "steps/s", "n_gpus": 0,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": 1.0 / step_s, "unit": "steps/s", "cores": samples[0]["cores"],
+                                 "kind": "oracle", "sample": samples[0]["sample"]},
+                "e2e": {"value": 1.0 / step_s, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    r = run_gpu(args, cfg, rank, world)
+    ms = r["ms"]
+    e2e_ms = r["e2e_ms"]
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms, e2e_ms / r["e2e_steps"]], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_per = float(t[0]), float(t[1])
+    else:
+        e2e_per = e2e_ms / r["e2e_steps"]
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    fp8_sustained = 2.0 * peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    K = args.steps
+    ms_step = ms / K
+    w_avg = statistics.mean(r["w_ms"]) if r["w_ms"] else float("nan")
+    a_avg = statistics.mean(r["a_ms"]) if r["a_ms"] else float("nan")
+    attn_tflops = attend_flop / (a_avg * 1e-3) / 1e12
+    write_gbs = write_bytes / (w_avg * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": world * K / (ms * 1e-3), "unit": "steps/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8_e4m3", "data": "synthetic", "config": config,
+        "e2e": {"value": world * 1e3 / e2e_per, "unit": "steps/s", "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"], "steps": r["e2e_steps"]},
+        "gpu_launches": r["launches"],
+        "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": fp8_sustained, "unit": "TFLOP/s",
+                     "frac": attn_tflops / fp8_sustained, "traffic": None,
+                     "kernel": "attention call (q-prep + attention + split combine)",
+                     "peak_source": f"{peak_src}: 2 x bf16_tflops_sustained (FP8 = 2 x bf16 nominal ratio)"},
+        "breakdown": {
+            "upkeep_ms_per_step": w_avg * L, "upkeep_gbs": write_gbs,
+            "upkeep_frac_hbm": write_gbs / peaks["hbm_gbs"],
+            "write_us_per_call": w_avg * 1e3,
+            "attend_us_per_call": a_avg * 1e3, "attend_tflops_per_call": attn_tflops,
+            "attend_ms_per_step": a_avg * L * P,
+            "attention_tflops_step": attend_flop * L * P / (a_avg * L * P * 1e-3) / 1e12,
+            "rebase_ms": r["rb_ms"],
+            "rebase_gbs": (rebase_bytes / (r["rb_ms"] * 1e-3) / 1e9) if r["rb_ms"] else None,
+            "hbm_peak_gbs": peaks["hbm_gbs"], "peaks": peak_src,
+        },
+        "clocks": r["clocks"],
+    }
+    if not args.no_cpu_baseline:
+        cb = oracle_sample(cfg)
+        line["cpu_baseline"] = {"value": 1.0 / cb["step_s"], "unit": "steps/s", "cores": cb["cores"],
+                                "kind": "oracle", "sample": cb["sample"]}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -147,6 +147,10 @@ int kvring_check_device(kvring_t* ring, void* cuda_stream);
  * kvring_create when ring is NULL).  Never NULL; valid until the next call. */
 const char* kvring_last_error(const kvring_t* ring);
 
+/* Number of kernels this ring has launched since it was created (every write,
+ * attend and rebase adds the launches it enqueued).  Errors: EINVAL. */
+int kvring_launch_count(const kvring_t* ring, uint64_t* out);
+
 /* Testing aid for the bounded waits: make the next kvring_attend skip the K/V
  * load of tile `skip_tile` (-1 = off) and give each device wait timeout_ns
  * nanoseconds (0 = default of 2 s).  The skipped load makes its consumer's wait

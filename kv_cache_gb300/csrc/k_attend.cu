@@ -126,7 +126,6 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
     float* sColV = sColK + 256;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::offBar);
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + L::offMisc);
-    volatile int* sFlag = reinterpret_cast<volatile int*>(smem + L::offMisc + 4);
     float* sRed = reinterpret_cast<float*>(smem + L::offMisc + 16);
 
     const int tid = threadIdx.x;
@@ -148,7 +147,6 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
     if (tid == 0) {
         for (int b = 0; b < 6; ++b) mbar_init(&bars[b], 1);
         fence_mbar_init();
-        *sFlag = 0;
         prefetch_tmap(&maps.q8);
         prefetch_tmap(&maps.k8);
         prefetch_tmap(&maps.vt8);
@@ -219,6 +217,7 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
             sColV[stage * 128 + tid] = valid ? __fmul_rn(scale_of(__ldg(vam + s)), inv_sv_ref) : 0.f;
         }
         // S = Q K^T
+        bool issue_failed = false;
         if (tid == 0) {
             bool ok = true;
             if (q_pending) {
@@ -237,11 +236,11 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                     mma_f8(tS, make_sdesc(aQ + k * 32, D), make_sdesc(aKs + k * 32, D), idS, k > 0 ? 1u : 0u);
                 mma_commit(&bars[kBarS]);
             } else {
-                *sFlag = 1;
+                issue_failed = true;
             }
         }
-        __syncthreads();
-        if (*sFlag) { aborted = true; break; }
+        // block-uniform abort decision
+        if (__syncthreads_or(issue_failed)) { aborted = true; break; }
 
         bool ok = mbar_wait(&bars[kBarS], (uint32_t)(it & 1), p.timeout_ns);
         if (!ok) record_timeout(p.err, kWaitS);
@@ -249,7 +248,7 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
             ok = mbar_wait(&bars[kBarO], (uint32_t)((it - 1) & 1), p.timeout_ns);
             if (!ok) record_timeout(p.err, kWaitO);
         }
-        if (!ok) *sFlag = 1;
+        const bool wait_failed = !ok;
         tc_fence_after();
 
         // widen the V tile to fp16 (exact): [D rows][128 slots] e4m3 -> 2 K-blocks of [D][64] fp16
@@ -290,11 +289,13 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                 if (col < nvalid) mt = fmaxf(mt, __uint_as_float(r[e]) * colK[col]);
             }
         }
-        if (m_run == -INFINITY) {
-            m_run = mt;
-        } else if ((mt - m_run) * a > 8.f) {
-            const float alpha = ex2_approx((m_run - mt) * a);
-            l_run *= alpha;
+        // Lazy rescale: move the running max only when it grows by more than 2^8.
+        // tcgen05.ld/st are warp-collective, so a warp rescales if any of its rows
+        // needs it; the other rows multiply by 1.
+        const bool first = m_run == -INFINITY;
+        const bool grow = !first && (mt - m_run) * a > 8.f;
+        if (__any_sync(0xffffffffu, grow)) {
+            const float alpha = grow ? ex2_approx((m_run - mt) * a) : 1.f;
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t r[32];
@@ -304,8 +305,9 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                 tmem_st32(tO + lane_off + cc * 32, r);
             }
             tmem_wait_st();
-            m_run = mt;
+            l_run *= alpha;
         }
+        if (first || grow) m_run = mt;
         const float ma = m_run * a;
         float lsum = 0.f;
         uint8_t* prow = sP16 + tid * 128;
@@ -336,8 +338,7 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
 
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();
-        if (*sFlag) { aborted = true; break; }
+        if (__syncthreads_or(wait_failed)) { aborted = true; break; }
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
@@ -356,37 +357,26 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
         bool ok = mbar_wait(&bars[kBarO], (uint32_t)((nt - 1) & 1), p.timeout_ns);
         if (!ok) { record_timeout(p.err, kWaitFinal); aborted = true; }
         tc_fence_after();
+        // every lane reads its TMEM row (warp-collective); only real rows are stored
         const int t = qt * 128 + tid;
-        if (ok && t < p.T) {
-            if (p.splits == 1) {
-                const float f = sv_ref / l_run;
-                float* dst = p.out + ((size_t)t * p.H + h) * D;
+        const bool store = ok && t < p.T;
+        const bool direct = p.splits == 1;
+        const float f = direct ? sv_ref / l_run : sv_ref;
+        const size_t prow_i = ((size_t)split * p.H + h) * p.Tstride + t;
+        float* dst = direct ? p.out + ((size_t)t * p.H + h) * D : p.part_o + prow_i * D;
 #pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t r[32];
-                    tmem_ld32(tO + lane_off + cc * 32, r);
+        for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t r[32];
+            tmem_ld32(tO + lane_off + cc * 32, r);
+            if (store) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4*>(dst + cc * 32 + e) =
-                            make_float4(__uint_as_float(r[e]) * f, __uint_as_float(r[e + 1]) * f,
-                                        __uint_as_float(r[e + 2]) * f, __uint_as_float(r[e + 3]) * f);
-                }
-            } else {
-                const size_t prow_i = ((size_t)split * p.H + h) * p.Tstride + t;
-                float* dst = p.part_o + prow_i * D;
-#pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t r[32];
-                    tmem_ld32(tO + lane_off + cc * 32, r);
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4*>(dst + cc * 32 + e) =
-                            make_float4(__uint_as_float(r[e]) * sv_ref, __uint_as_float(r[e + 1]) * sv_ref,
-                                        __uint_as_float(r[e + 2]) * sv_ref, __uint_as_float(r[e + 3]) * sv_ref);
-                }
-                *reinterpret_cast<float2*>(p.part_ml + prow_i * 2) = make_float2(m_run * a, l_run);
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4*>(dst + cc * 32 + e) =
+                        make_float4(__uint_as_float(r[e]) * f, __uint_as_float(r[e + 1]) * f,
+                                    __uint_as_float(r[e + 2]) * f, __uint_as_float(r[e + 3]) * f);
             }
         }
+        if (store && !direct) *reinterpret_cast<float2*>(p.part_ml + prow_i * 2) = make_float2(m_run * a, l_run);
     }
     if (aborted && tid == 0) {
         // drain: every MMA this thread issued, then every TMA copy still in flight

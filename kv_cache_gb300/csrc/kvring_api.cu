@@ -55,6 +55,7 @@ struct kvring {
     int* err = nullptr;         // [4]
     AttendMaps maps{};
     // testing aid
+    uint64_t launches = 0;
     int debug_skip_tile = -1;
     long long debug_timeout_ns = 0;
     std::string error;
@@ -289,6 +290,7 @@ int kvring_write(kvring_t* r, int32_t layer, const void* k, const void* v, int32
         p.groups = groups;
         cudaError_t e = launch_write(p, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(r, e, "write kernel launch");
+        r->launches += 1;
     }
     for (int j = 0; j < n; ++j) {
         const int64_t slot = (L.head + j) % R;
@@ -332,6 +334,7 @@ int kvring_attend(kvring_t* r, int32_t layer, const void* q, int32_t n_q, float*
     qp.Tstride = (int)r->Tstride;
     cudaError_t e = launch_qprep(qp, s);
     if (e != cudaSuccess) return cuda_fail(r, e, "q-prep kernel launch");
+    r->launches += 1;
 
     AttendParams ap{};
     const size_t lh = (size_t)layer * H;
@@ -361,6 +364,7 @@ int kvring_attend(kvring_t* r, int32_t layer, const void* q, int32_t n_q, float*
     r->debug_timeout_ns = 0;
     e = launch_attend(ap, r->maps, s);
     if (e != cudaSuccess) return cuda_fail(r, e, "attention kernel launch");
+    r->launches += 1;
     if (ap.splits > 1) {
         CombineParams cp{};
         cp.part_o = r->part_o;
@@ -373,6 +377,7 @@ int kvring_attend(kvring_t* r, int32_t layer, const void* q, int32_t n_q, float*
         cp.splits = ap.splits;
         e = launch_combine(cp, s);
         if (e != cudaSuccess) return cuda_fail(r, e, "combine kernel launch");
+        r->launches += 1;
     }
     return KVRING_OK;
 }
@@ -399,6 +404,7 @@ int kvring_rebase(kvring_t* r, void* stream) {
         p.Rpad = (int)r->Rpad;
         cudaError_t e = launch_rebase(p, r->num_sms, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(r, e, "rebase kernel launch");
+        r->launches += 1;
     }
     for (int l = 0; l < c.num_layers; ++l) {
         LayerState& L = r->layers[l];
@@ -482,6 +488,12 @@ int kvring_check_device(kvring_t* r, void* stream) {
 const char* kvring_last_error(const kvring_t* r) {
     if (!r) return g_create_error.c_str();
     return r->error.c_str();
+}
+
+int kvring_launch_count(const kvring_t* r, uint64_t* out) {
+    if (!r || !out) return KVRING_EINVAL;
+    *out = r->launches;
+    return KVRING_OK;
 }
 
 int kvring_debug_fault(kvring_t* r, int32_t skip_tile, int64_t timeout_ns) {

@@ -82,6 +82,7 @@ _SIGNATURES = {
     "kvring_check_device": (ctypes.c_int, [_P, _P]),
     "kvring_last_error": (ctypes.c_char_p, [_P]),
     "kvring_debug_fault": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int64]),
+    "kvring_launch_count": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint64)]),
 }
 
 
@@ -192,6 +193,12 @@ def kvring_last_error(ring) -> str:
     return msg.decode() if msg else ""
 
 
+def kvring_launch_count(ring) -> int:
+    n = ctypes.c_uint64()
+    _check(load().kvring_launch_count(ring, ctypes.byref(n)), ring)
+    return int(n.value)
+
+
 def kvring_debug_fault(ring, skip_tile: int, timeout_ns: int) -> None:
     _check(load().kvring_debug_fault(ring, skip_tile, timeout_ns), ring)
 
@@ -247,3 +254,6 @@ class KVRing:
 
     def check_device(self, stream=None) -> int:
         return kvring_check_device(self.handle, stream)
+
+    def launch_count(self) -> int:
+        return kvring_launch_count(self.handle)
