@@ -63,7 +63,7 @@ typedef struct {
     int32_t  num_heads;              /* H: 1..256                                            */
     int32_t  head_dim;               /* d: 64 or 128                                         */
     int32_t  capacity;               /* R: slots per ring, 1..1048576                        */
-    int32_t  max_tokens_per_write;   /* T_max: 1..capacity                                   */
+    int32_t  max_tokens_per_write;   /* T_max: 1..min(capacity, 2048)                        */
     int32_t  max_position;           /* positions must stay below this; 0 -> 65536.  Sets the
                                         size of the RoPE table (max_position x d/2 x 8 bytes) */
     float    rope_theta;             /* RoPE base; 0 -> 10000                                */

@@ -80,320 +80,505 @@ cudaError_t launch_qprep(const QPrepParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+
 // ============================================================== K4: attention
+// One CTA of 14 warps per (head, pair of 128-row query tiles, KV split):
+//   warps 0-3   softmax for query tile 0 (tensor-memory lanes 0-127 of S0, O0)
+//   warps 4-7   softmax for query tile 1 (S1, O1)
+//   warps 8-11  widen each V tile from e4m3 to fp16 (exact)
+//   warp 12     TMA producer (Q tiles once, then K/V tiles through 2 stages)
+//   warp 13     tcgen05 issuer: S_q(j+1) = Q_q K_{j+1}^T goes out before
+//               O_q += P_q(j) V_j, so each softmax group finds its next S ready
+// Tensor memory (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [384,384+d).
+// The two query tiles share every K/V tile, halving K/V shared-memory traffic
+// per FLOP.  Hand-offs are mbarriers; every wait is bounded and also gives up
+// as soon as another warp has recorded a time-out.
 template <int D>
 struct AttendSmem {
-    static constexpr int kQ = 128 * D;            // Q tile, e4m3
-    static constexpr int kK = 128 * D;            // K tile, e4m3 (per stage)
-    static constexpr int kV = D * 128;            // V tile [d][128 slots], e4m3 (per stage)
-    static constexpr int kV16 = D * 128 * 2;      // V tile widened to fp16: 2 K-blocks of [D][64]
-    static constexpr int kP16 = 128 * 128 * 2;    // P fp16: 2 K-blocks of [128][64]
+    static constexpr int kStages = 2;
+    static constexpr int kQ = 128 * D;            // one query tile, e4m3
+    static constexpr int kK = 128 * D;            // K tile [128 slots][D], e4m3
+    static constexpr int kV = D * 128;            // V tile [D][128 slots], e4m3
+    static constexpr int kV16 = D * 128 * 2;      // V tile in fp16: 2 K-blocks of [D][64]
+    static constexpr int kP = 128 * 128 * 2;      // P in fp16: 2 K-blocks of [128][64]
     static constexpr int offQ = 0;
-    static constexpr int offK = offQ + kQ;
-    static constexpr int offV = offK + 2 * kK;
-    static constexpr int offV16 = offV + 2 * kV;
-    static constexpr int offP16 = offV16 + kV16;
-    static constexpr int offCol = offP16 + kP16;               // float colK[2][128], colV[2][128]
-    static constexpr int offBar = offCol + 4 * 128 * 4;        // 8 mbarriers
-    static constexpr int offMisc = offBar + 8 * 8;             // tmem addr, flag, reductions
+    static constexpr int offK = offQ + 2 * kQ;
+    static constexpr int offV = offK + kStages * kK;
+    static constexpr int offV16 = offV + kStages * kV;
+    static constexpr int offP = offV16 + 2 * kV16;
+    static constexpr int offBar = offP + 2 * kP;
+    static constexpr int kBars = 16;
+    static constexpr int offMisc = offBar + kBars * 8;
     static constexpr int kBytes = offMisc + 64;
-    static constexpr int kAlloc = kBytes + 1024;               // slack for 1024-byte alignment
+    static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
-enum : int { kBarQ = 0, kBarKV0 = 1, kBarKV1 = 2, kBarS = 3, kBarO = 4, kBarDrain = 5 };
-enum : int { kWaitQ = 1, kWaitKV = 2, kWaitS = 3, kWaitO = 4, kWaitFinal = 5 };
+// mbarrier slots
+enum : int {
+    kBQ = 0,        // Q tiles landed (TMA)
+    kBKVF = 1,      // [2] K/V stage full (TMA)
+    kBKVE = 3,      // [2] K/V stage free: S MMAs done (commit) + 128 converter arrivals
+    kBSF = 5,       // [2] S_q computed (commit)
+    kBPF = 7,       // [2] P_q written and S_q read (128 softmax arrivals)
+    kBOF = 9,       // [2] O_q += P_q V done (commit)
+    kBVF = 11,      // [2] fp16 V buffer full (128 converter arrivals)
+    kBVE = 13,      // [2] fp16 V buffer free (commit after both PV MMAs)
+    kBDrain = 15,   // drain after an abort
+};
+enum : int { kWaitQ = 1, kWaitKVFull = 2, kWaitKVEmpty = 3, kWaitS = 4, kWaitP = 5, kWaitO = 6, kWaitV16Full = 7,
+             kWaitV16Empty = 8 };
+constexpr int kAttendThreads = 448;
 
-__device__ __forceinline__ void record_timeout(int* err, int site) {
-    if (atomicCAS(err, 0, KVRING_ETIMEOUT) == 0) {
-        err[1] = kKernelAttend;
-        err[2] = site;
-        err[3] = (int)blockIdx.x;
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Warp-collective bounded wait: lane 0 polls, the verdict is broadcast.  Gives
+// up when the phase does not complete within timeout_ns (and then records the
+// time-out and raises the CTA's abort flag) or when the abort flag is raised.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          const AttendParams& p, int site) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) {
+        if (!mbar_try_wait(bar, parity)) {
+            uint64_t t0 = globaltimer_ns();
+            while (true) {
+                if (mbar_try_wait(bar, parity)) break;
+                if (*abort_flag) { ok = 0; break; }
+                if ((long long)(globaltimer_ns() - t0) > p.timeout_ns) {
+                    *abort_flag = 1;
+                    if (atomicCAS(p.err, 0, KVRING_ETIMEOUT) == 0) {
+                        p.err[1] = kKernelAttend;
+                        p.err[2] = site;
+                        p.err[3] = (int)blockIdx.x;
+                    }
+                    ok = 0;
+                    break;
+                }
+            }
+        }
     }
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 template <int D>
-__global__ void __launch_bounds__(128, 1)
+__device__ __forceinline__ void issue_s(uint32_t tS, uint32_t aQ, uint32_t aK) {
+    constexpr uint32_t id = make_idesc(128, 128);
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k)
+        mma_f8(tS, make_sdesc(aQ + k * 32, D), make_sdesc(aK + k * 32, D), id, k > 0 ? 1u : 0u);
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t aP, uint32_t aV16, bool accumulate) {
+    constexpr uint32_t id = make_idesc(128, D);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t offp = (k >> 2) * (128 * 128) + (k & 3) * 32;
+        const uint32_t offv = (k >> 2) * (D * 128) + (k & 3) * 32;
+        mma_f16(tO, make_sdesc(aP + offp, 128), make_sdesc(aV16 + offv, 128), id, (accumulate || k > 0) ? 1u : 0u);
+    }
+}
+
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAttendThreads, 1)
 attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ AttendMaps maps) {
     using L = AttendSmem<D>;
+    constexpr int NST = L::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem + L::offQ;
     uint8_t* sK = smem + L::offK;
     uint8_t* sV = smem + L::offV;
     uint8_t* sV16 = smem + L::offV16;
-    uint8_t* sP16 = smem + L::offP16;
-    float* sColK = reinterpret_cast<float*>(smem + L::offCol);
-    float* sColV = sColK + 256;
+    uint8_t* sP = smem + L::offP;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::offBar);
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + L::offMisc);
+    volatile int* sAbort = reinterpret_cast<volatile int*>(smem + L::offMisc + 4);
+    volatile int* sLast = reinterpret_cast<volatile int*>(smem + L::offMisc + 8);
     float* sRed = reinterpret_cast<float*>(smem + L::offMisc + 16);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
 
-    // ---- unit of work
-    int unit = blockIdx.x;
-    const int split = unit % p.splits;
-    unit /= p.splits;
-    const int qt = unit % p.qtiles;
-    const int h = unit / p.qtiles;
+    int u = blockIdx.x;
+    const int split = u % p.splits;
+    u /= p.splits;
+    const int pair = u % p.npairs;
+    const int h = u / p.npairs;
     const int j0 = split * p.tiles_per_split;
-    const int j1 = min(p.ntiles, j0 + p.tiles_per_split);
-    const int nt = j1 - j0;
-    const int zrow = p.layer * p.H + h;          // (layer, head) row of the ring tensor maps
-
-    if (warp == 0) tmem_alloc(sTmem, 256);
-    if (tid == 0) {
-        for (int b = 0; b < 6; ++b) mbar_init(&bars[b], 1);
-        fence_mbar_init();
-        prefetch_tmap(&maps.q8);
-        prefetch_tmap(&maps.k8);
-        prefetch_tmap(&maps.vt8);
-    }
-
-    // V scale reference: largest V scale among this split's valid slots
-    const float* vam = p.vamax + (size_t)h * p.Rpad;
+    const int nt = min(p.ntiles, j0 + p.tiles_per_split) - j0;
+    const int nq = ((2 * pair + 1) * 128 < p.T) ? 2 : 1;
+    const int zrow = p.layer * p.H + h;
     const float* kam = p.kamax + (size_t)h * p.Rpad;
-    const int s_end = min(j1 * 128, p.count);
-    float svmax = 0.f;
-    for (int s = j0 * 128 + tid; s < s_end; s += 128) svmax = fmaxf(svmax, scale_of(__ldg(vam + s)));
-#pragma unroll
-    for (int off = 16; off; off >>= 1) svmax = fmaxf(svmax, __shfl_xor_sync(0xffffffffu, svmax, off));
-    if (lane == 0) sRed[warp] = svmax;
+    const float* vam = p.vamax + (size_t)h * p.Rpad;
 
+    if (warp == 0) tmem_alloc(sTmem, 512);
+    if (tid == 0) {
+        const int counts[L::kBars] = {1, 1, 1, 129, 129, 1, 1, 128, 128, 1, 1, 128, 128, 1, 1, 1};
+        for (int b = 0; b < L::kBars; ++b) mbar_init(&bars[b], counts[b]);
+        fence_mbar_init();
+        *sAbort = 0;
+        *sLast = 0;
+    }
+    // V scale reference of this split: largest V scale among its valid slots (converter warps)
+    if (warp >= 8 && warp < 12) {
+        const int c = tid - 256;
+        const int s_end = min((j0 + nt) * 128, p.count);
+        float m = 0.f;
+        for (int s = j0 * 128 + c; s < s_end; s += 128) m = fmaxf(m, scale_of(__ldg(vam + s)));
+#pragma unroll
+        for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if (lane == 0) sRed[warp - 8] = m;
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    const uint32_t tmem = *sTmem;
     const float sv_ref = fmaxf(fmaxf(sRed[0], sRed[1]), fmaxf(sRed[2], sRed[3]));
     const float inv_sv_ref = __frcp_rn(sv_ref);
-    const uint32_t tmem = *sTmem;
-    const uint32_t tS = tmem;                     // columns [0, 128): S, fp32
-    const uint32_t tO = tmem + 128;               // columns [128, 128 + D): O, fp32
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
 
-    // row constants: a = (Q row scale) * log2(e) / sqrt(d)
-    const int qrow = qt * 128 + tid;
-    const float qa = __ldg(p.qamax + (size_t)h * p.Tstride + qrow);
-    const float a = scale_of(qa) * p.log2e_rsqrt_d;
+    // softmax state (warps 0-7), kept for the epilogue
+    const int q = warp >> 2;                     // query tile of a softmax warp
+    const int wq = warp & 3;
+    const int row = tid & 127;
+    const int qrow = (2 * pair + q) * 128 + row;
+    float m_run = -INFINITY, l_run = 0.f, a = 0.f;
+    // producer state (warp 12, lane 0)
+    int issued[NST];
+#pragma unroll
+    for (int st = 0; st < NST; ++st) issued[st] = 0;
+    bool q_issued = false;
 
-    // producer state (thread 0 only)
-    int issued[2] = {0, 0}, consumed[2] = {0, 0};
-    bool q_pending = false;
-    auto issue_kv = [&](int stage, int j) {
-        if (j == p.skip_tile) return;             // testing aid: leave this load out
-        uint64_t* bar = &bars[kBarKV0 + stage];
-        mbar_expect_tx(bar, (uint32_t)(L::kK + L::kV));
-        tma_load_3d(sK + stage * L::kK, &maps.k8, bar, 0, j * 128, zrow);
-        tma_load_3d(sV + stage * L::kV, &maps.vt8, bar, j * 128, 0, zrow);
-        issued[stage]++;
-    };
-    if (tid == 0) {
-        mbar_expect_tx(&bars[kBarQ], (uint32_t)L::kQ);
-        tma_load_3d(sQ, &maps.q8, &bars[kBarQ], 0, qt * 128, h);
-        q_pending = true;
-        for (int st = 0; st < 2 && st < nt; ++st) issue_kv(st, j0 + st);
-    }
-
-    constexpr uint32_t idS = make_idesc(128, 128);
-    constexpr uint32_t idO = make_idesc(128, D);
-    const uint32_t aQ = smem_u32(sQ);
-    const uint32_t aK = smem_u32(sK);
-    const uint32_t aP = smem_u32(sP16);
-    const uint32_t aV16 = smem_u32(sV16);
-
-    float m_run = -INFINITY;
-    float l_run = 0.f;
-    bool aborted = false;
-
-    for (int it = 0; it < nt; ++it) {
-        const int stage = it & 1;
-        const int j = j0 + it;
-        // per-slot scales of this tile (slots past count are masked below)
-        {
-            const int s = j * 128 + tid;
-            const bool valid = s < p.count;
-            sColK[stage * 128 + tid] = valid ? scale_of(__ldg(kam + s)) : 0.f;
-            sColV[stage * 128 + tid] = valid ? __fmul_rn(scale_of(__ldg(vam + s)), inv_sv_ref) : 0.f;
-        }
-        // S = Q K^T
-        bool issue_failed = false;
-        if (tid == 0) {
-            bool ok = true;
-            if (q_pending) {
-                ok = mbar_wait(&bars[kBarQ], 0, p.timeout_ns);
-                if (ok) q_pending = false; else record_timeout(p.err, kWaitQ);
+    if (warp < 8) {
+        // ------------------------------------------------------------ softmax
+        const bool active = q < nq;
+        const uint32_t tS = tmem + 128 * q;
+        const uint32_t tO = tmem + 256 + 128 * q;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        a = scale_of(__ldg(p.qamax + (size_t)h * p.Tstride + qrow)) * p.log2e_rsqrt_d;
+        uint8_t* prow = sP + q * L::kP + row * 128;
+        for (int it = 0; active && it < nt; ++it) {
+            const int j = j0 + it;
+            const int nvalid = min(128, p.count - j * 128);
+            // per-slot scales of this tile, four 32-column groups; lane e holds column 32g + e
+            float ksv[4], rv[4], KS[4], RR[4], RI[4];
+            bool uni[4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const int col = g * 32 + lane;
+                const bool valid = col < nvalid;
+                ksv[g] = valid ? scale_of(__ldg(kam + j * 128 + col)) : 0.f;
+                rv[g] = valid ? __fmul_rn(scale_of(__ldg(vam + j * 128 + col)), inv_sv_ref) : 0.f;
+                KS[g] = __shfl_sync(0xffffffffu, ksv[g], 0);
+                RR[g] = __shfl_sync(0xffffffffu, rv[g], 0);
+                uni[g] = __all_sync(0xffffffffu, valid && ksv[g] == KS[g] && rv[g] == RR[g]);
+                RI[g] = uni[g] ? __frcp_rn(RR[g]) : 0.f;
             }
-            if (ok) {
-                ok = mbar_wait(&bars[kBarKV0 + stage], (uint32_t)(consumed[stage] & 1), p.timeout_ns);
-                if (ok) consumed[stage]++; else record_timeout(p.err, kWaitKV);
+            if (!warp_wait(&bars[kBSF + q], (uint32_t)(it & 1), sAbort, p, kWaitS)) break;
+            tc_fence_after();
+            // pass 1: row max of raw * k_scale
+            float tm = -INFINITY;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                uint32_t r[32];
+                tmem_ld32(tS + lane_off + g * 32, r);
+                if (uni[g]) {
+                    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        m0 = fmaxf(m0, __uint_as_float(r[e]));
+                        m1 = fmaxf(m1, __uint_as_float(r[e + 1]));
+                        m2 = fmaxf(m2, __uint_as_float(r[e + 2]));
+                        m3 = fmaxf(m3, __uint_as_float(r[e + 3]));
+                    }
+                    tm = fmaxf(tm, fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * KS[g]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float ks = __shfl_sync(0xffffffffu, ksv[g], e);
+                        if (g * 32 + e < nvalid) tm = fmaxf(tm, __uint_as_float(r[e]) * ks);
+                    }
+                }
             }
-            if (ok) {
+            // P_q buffer and O_q are free once O_q += P_q(j-1) V has finished
+            if (it > 0) {
+                if (!warp_wait(&bars[kBOF + q], (uint32_t)((it - 1) & 1), sAbort, p, kWaitO)) break;
                 tc_fence_after();
-                const uint32_t aKs = aK + stage * L::kK;
-#pragma unroll
-                for (int k = 0; k < D / 32; ++k)
-                    mma_f8(tS, make_sdesc(aQ + k * 32, D), make_sdesc(aKs + k * 32, D), idS, k > 0 ? 1u : 0u);
-                mma_commit(&bars[kBarS]);
-            } else {
-                issue_failed = true;
             }
-        }
-        // block-uniform abort decision
-        if (__syncthreads_or(issue_failed)) { aborted = true; break; }
-
-        bool ok = mbar_wait(&bars[kBarS], (uint32_t)(it & 1), p.timeout_ns);
-        if (!ok) record_timeout(p.err, kWaitS);
-        if (ok && it > 0) {
-            ok = mbar_wait(&bars[kBarO], (uint32_t)((it - 1) & 1), p.timeout_ns);
-            if (!ok) record_timeout(p.err, kWaitO);
-        }
-        const bool wait_failed = !ok;
-        tc_fence_after();
-
-        // widen the V tile to fp16 (exact): [D rows][128 slots] e4m3 -> 2 K-blocks of [D][64] fp16
-        {
-            const uint8_t* src = sV + stage * L::kV;
+            // lazy rescale: move the running max only when it grows by more than 2^8
+            const bool first = m_run == -INFINITY;
+            const bool grow = !first && (tm - m_run) * a > 8.f;
+            if (__any_sync(0xffffffffu, grow)) {
+                const float alpha = grow ? ex2_approx((m_run - tm) * a) : 1.f;
 #pragma unroll
-            for (int q = tid; q < D * 8; q += 128) {
-                const int dd = q >> 3, c = q & 7;
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t r[32];
+                    tmem_ld32(tO + lane_off + cc * 32, r);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                    tmem_st32(tO + lane_off + cc * 32, r);
+                }
+                tmem_wait_st();
+                l_run *= alpha;
+            }
+            if (first || grow) m_run = tm;
+            const float ma = m_run * a;
+            // pass 2: P = 2^(x - m) * (V scale / reference), fp16, into shared memory.
+            // The row sum uses the rounded P (over the V ratio), the same weights the
+            // P V product sees, so the rounding of a dominant weight cancels.
+            float lsum = 0.f;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                uint32_t r[32];
+                tmem_ld32(tS + lane_off + g * 32, r);
+                uint32_t pk[16];
+                if (uni[g]) {
+                    const float c1 = KS[g] * a;
+                    const float c0 = lg2_approx(RR[g]) - ma;
+                    float lg0 = 0.f, lg1 = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const float p0 = ex2_approx(fmaf(__uint_as_float(r[e]), c1, c0));
+                        const float p1 = ex2_approx(fmaf(__uint_as_float(r[e + 1]), c1, c0));
+                        const __half2 hv = __floats2half2_rn(p0, p1);
+                        pk[e / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+                        const float2 back = __half22float2(hv);
+                        lg0 += back.x;
+                        lg1 += back.y;
+                    }
+                    lsum += (lg0 + lg1) * RI[g];
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const float ks0 = __shfl_sync(0xffffffffu, ksv[g], e);
+                        const float ks1 = __shfl_sync(0xffffffffu, ksv[g], e + 1);
+                        const float r0 = __shfl_sync(0xffffffffu, rv[g], e);
+                        const float r1 = __shfl_sync(0xffffffffu, rv[g], e + 1);
+                        const bool v0 = g * 32 + e < nvalid, v1 = g * 32 + e + 1 < nvalid;
+                        const float p0 = v0 ? ex2_approx(fmaf(__uint_as_float(r[e]) * ks0, a, -ma)) * r0 : 0.f;
+                        const float p1 = v1 ? ex2_approx(fmaf(__uint_as_float(r[e + 1]) * ks1, a, -ma)) * r1 : 0.f;
+                        const __half2 hv = __floats2half2_rn(p0, p1);
+                        pk[e / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+                        const float2 back = __half22float2(hv);
+                        if (v0) lsum += __fdiv_rn(back.x, r0);
+                        if (v1) lsum += __fdiv_rn(back.y, r1);
+                    }
+                }
+                uint8_t* blk = prow + (g >> 1) * (128 * 128);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int cb = (g & 1) * 4 + c;
+                    *reinterpret_cast<uint4*>(blk + ((cb ^ (row & 7)) << 4)) =
+                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                }
+            }
+            l_run += lsum;
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bars[kBPF + q]);
+        }
+        if (active && !*sAbort) {
+            if (warp_wait(&bars[kBOF + q], (uint32_t)((nt - 1) & 1), sAbort, p, kWaitO)) tc_fence_after();
+        }
+    } else if (warp < 12) {
+        // ------------------------------------------------------------ V e4m3 -> fp16
+        const int c0 = tid - 256;
+        for (int it = 0; it < nt; ++it) {
+            const int st = it % NST, b = it & 1;
+            if (!warp_wait(&bars[kBKVF + st], (uint32_t)((it / NST) & 1), sAbort, p, kWaitKVFull)) break;
+            if (it >= 2 && !warp_wait(&bars[kBVE + b], (uint32_t)(((it >> 1) - 1) & 1), sAbort, p, kWaitV16Empty)) break;
+            const uint8_t* src = sV + st * L::kV;
+            uint8_t* dst = sV16 + b * L::kV16;
+#pragma unroll
+            for (int qq = c0; qq < D * 8; qq += 128) {
+                const int dd = qq >> 3, c = qq & 7;
                 const uint4 w = *reinterpret_cast<const uint4*>(src + dd * 128 + ((c ^ (dd & 7)) << 4));
                 const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
                 uint32_t h16[8];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(ws[e] & 0xFFFFu), __NV_E4M3);
-                    __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(ws[e] >> 16), __NV_E4M3);
+                    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(ws[e] & 0xFFFFu), __NV_E4M3);
+                    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(ws[e] >> 16), __NV_E4M3);
                     h16[2 * e] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
                     h16[2 * e + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
                 }
-                uint8_t* dblk = sV16 + (c >> 2) * (D * 128) + dd * 128;
+                uint8_t* dblk = dst + (c >> 2) * (D * 128) + dd * 128;
                 const int cb = (c & 3) * 2;
                 *reinterpret_cast<uint4*>(dblk + (((cb + 0) ^ (dd & 7)) << 4)) = make_uint4(h16[0], h16[1], h16[2], h16[3]);
                 *reinterpret_cast<uint4*>(dblk + (((cb + 1) ^ (dd & 7)) << 4)) = make_uint4(h16[4], h16[5], h16[6], h16[7]);
             }
+            fence_proxy_async_smem();
+            mbar_arrive(&bars[kBVF + b]);
+            mbar_arrive(&bars[kBKVE + st]);
         }
-
-        // softmax on row tid
-        const int nvalid = min(128, p.count - j * 128);
-        const float* colK = sColK + stage * 128;
-        const float* colV = sColV + stage * 128;
-        float mt = -INFINITY;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            uint32_t r[32];
-            tmem_ld32(tS + lane_off + cc * 32, r);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int col = cc * 32 + e;
-                if (col < nvalid) mt = fmaxf(mt, __uint_as_float(r[e]) * colK[col]);
+    } else if (warp == 12) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&maps.q8);
+            prefetch_tmap(&maps.k8);
+            prefetch_tmap(&maps.vt8);
+            mbar_expect_tx(&bars[kBQ], (uint32_t)(nq * L::kQ));
+            tma_load_3d(sQ, &maps.q8, &bars[kBQ], 0, (2 * pair) * 128, h);
+            if (nq == 2) tma_load_3d(sQ + L::kQ, &maps.q8, &bars[kBQ], 0, (2 * pair + 1) * 128, h);
+            q_issued = true;
+        }
+        for (int it = 0; it < nt; ++it) {
+            const int st = it % NST;
+            if (it >= NST && !warp_wait(&bars[kBKVE + st], (uint32_t)(((it / NST) - 1) & 1), sAbort, p, kWaitKVEmpty))
+                break;
+            const int j = j0 + it;
+            if (lane == 0 && j != p.skip_tile) {
+                mbar_expect_tx(&bars[kBKVF + st], (uint32_t)(L::kK + L::kV));
+                tma_load_3d(sK + st * L::kK, &maps.k8, &bars[kBKVF + st], 0, j * 128, zrow);
+                tma_load_3d(sV + st * L::kV, &maps.vt8, &bars[kBKVF + st], j * 128, 0, zrow);
+                issued[st]++;
+            }
+            __syncwarp();
+        }
+    } else {
+        // ------------------------------------------------------------ MMA issuer
+        const uint32_t aQ = smem_u32(sQ);
+        const uint32_t aK = smem_u32(sK);
+        const uint32_t aP = smem_u32(sP);
+        const uint32_t aV16 = smem_u32(sV16);
+        bool ok = warp_wait(&bars[kBQ], 0, sAbort, p, kWaitQ) && warp_wait(&bars[kBKVF], 0, sAbort, p, kWaitKVFull);
+        if (ok) {
+            tc_fence_after();
+            if (lane == 0) {
+                for (int qq = 0; qq < nq; ++qq) {
+                    issue_s<D>(tmem + 128 * qq, aQ + qq * L::kQ, aK);
+                    mma_commit(&bars[kBSF + qq]);
+                }
+                mma_commit(&bars[kBKVE]);
+            }
+            __syncwarp();
+        }
+        for (int it = 0; ok && it < nt; ++it) {
+            const int stn = (it + 1) % NST, b = it & 1;
+            for (int qq = 0; qq < nq && ok; ++qq) {
+                ok = warp_wait(&bars[kBPF + qq], (uint32_t)(it & 1), sAbort, p, kWaitP);
+                if (!ok) break;
+                tc_fence_after();
+                if (it + 1 < nt) {
+                    if (qq == 0) {
+                        ok = warp_wait(&bars[kBKVF + stn], (uint32_t)(((it + 1) / NST) & 1), sAbort, p, kWaitKVFull);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    if (lane == 0) {
+                        issue_s<D>(tmem + 128 * qq, aQ + qq * L::kQ, aK + stn * L::kK);
+                        mma_commit(&bars[kBSF + qq]);
+                        if (qq == nq - 1) mma_commit(&bars[kBKVE + stn]);
+                    }
+                    __syncwarp();
+                }
+                if (qq == 0) {
+                    ok = warp_wait(&bars[kBVF + b], (uint32_t)((it >> 1) & 1), sAbort, p, kWaitV16Full);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                if (lane == 0) {
+                    issue_pv<D>(tmem + 256 + 128 * qq, aP + qq * L::kP, aV16 + b * L::kV16, it > 0);
+                    mma_commit(&bars[kBOF + qq]);
+                    if (qq == nq - 1) mma_commit(&bars[kBVE + b]);
+                }
+                __syncwarp();
             }
         }
-        // Lazy rescale: move the running max only when it grows by more than 2^8.
-        // tcgen05.ld/st are warp-collective, so a warp rescales if any of its rows
-        // needs it; the other rows multiply by 1.
-        const bool first = m_run == -INFINITY;
-        const bool grow = !first && (mt - m_run) * a > 8.f;
-        if (__any_sync(0xffffffffu, grow)) {
-            const float alpha = grow ? ex2_approx((m_run - mt) * a) : 1.f;
+    }
+
+    // ---------------------------------------------------------------- join
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const bool aborted = *sAbort != 0;
+    if (aborted) {
+        // nothing of ours may still be in flight when the CTA exits
+        if (warp == 13 && lane == 0) {
+            mma_commit(&bars[kBDrain]);
+            mbar_wait(&bars[kBDrain], 0, p.timeout_ns);
+        }
+        if (warp == 12 && lane == 0) {
+            if (q_issued) mbar_wait(&bars[kBQ], 0, p.timeout_ns);
+            for (int st = 0; st < NST; ++st)
+                if (issued[st] > 0) mbar_wait(&bars[kBKVF + st], (uint32_t)((issued[st] - 1) & 1), p.timeout_ns);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        if (warp < 8 && q < nq) {
+            const uint32_t tO = tmem + 256 + 128 * q;
+            const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+            const bool store = qrow < p.T;
+            const bool direct = p.splits == 1;
+            const float f = direct ? sv_ref / l_run : sv_ref;
+            const size_t prow_i = ((size_t)split * p.H + h) * p.Tstride + qrow;
+            float* dst = direct ? p.out + ((size_t)qrow * p.H + h) * D : p.part_o + prow_i * D;
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t r[32];
                 tmem_ld32(tO + lane_off + cc * 32, r);
+                if (store) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                tmem_st32(tO + lane_off + cc * 32, r);
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4*>(dst + cc * 32 + e) =
+                            make_float4(__uint_as_float(r[e]) * f, __uint_as_float(r[e + 1]) * f,
+                                        __uint_as_float(r[e + 2]) * f, __uint_as_float(r[e + 3]) * f);
+                }
             }
-            tmem_wait_st();
-            l_run *= alpha;
-        }
-        if (first || grow) m_run = mt;
-        const float ma = m_run * a;
-        float lsum = 0.f;
-        uint8_t* prow = sP16 + tid * 128;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            uint32_t r[32];
-            tmem_ld32(tS + lane_off + cc * 32, r);
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-                const int col = cc * 32 + e;
-                float p0 = 0.f, p1 = 0.f;
-                if (col < nvalid) p0 = ex2_approx(fmaf(__uint_as_float(r[e]) * colK[col], a, -ma));
-                if (col + 1 < nvalid) p1 = ex2_approx(fmaf(__uint_as_float(r[e + 1]) * colK[col + 1], a, -ma));
-                lsum += p0 + p1;
-                __half2 hv = __floats2half2_rn(p0 * colV[col], p1 * colV[col + 1]);
-                pk[e / 2] = *reinterpret_cast<uint32_t*>(&hv);
-            }
-            uint8_t* blk = prow + (cc >> 1) * (128 * 128);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int cb = (cc & 1) * 4 + q;
-                *reinterpret_cast<uint4*>(blk + ((cb ^ (tid & 7)) << 4)) =
-                    make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            }
-        }
-        l_run += lsum;
-
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(wait_failed)) { aborted = true; break; }
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t off = (k >> 2) * (128 * 128) + (k & 3) * 32;
-                const uint32_t offv = (k >> 2) * (D * 128) + (k & 3) * 32;
-                mma_f16(tO, make_sdesc(aP + off, 128), make_sdesc(aV16 + offv, 128), idO,
-                        (it > 0 || k > 0) ? 1u : 0u);
-            }
-            mma_commit(&bars[kBarO]);
-            if (it + 2 < nt) issue_kv(stage, j0 + it + 2);
+            if (store && !direct) *reinterpret_cast<float2*>(p.part_ml + prow_i * 2) = make_float2(m_run * a, l_run);
         }
     }
-
-    if (!aborted) {
-        bool ok = mbar_wait(&bars[kBarO], (uint32_t)((nt - 1) & 1), p.timeout_ns);
-        if (!ok) { record_timeout(p.err, kWaitFinal); aborted = true; }
-        tc_fence_after();
-        // every lane reads its TMEM row (warp-collective); only real rows are stored
-        const int t = qt * 128 + tid;
-        const bool store = ok && t < p.T;
-        const bool direct = p.splits == 1;
-        const float f = direct ? sv_ref / l_run : sv_ref;
-        const size_t prow_i = ((size_t)split * p.H + h) * p.Tstride + t;
-        float* dst = direct ? p.out + ((size_t)t * p.H + h) * D : p.part_o + prow_i * D;
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t r[32];
-            tmem_ld32(tO + lane_off + cc * 32, r);
-            if (store) {
-#pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    *reinterpret_cast<float4*>(dst + cc * 32 + e) =
-                        make_float4(__uint_as_float(r[e]) * f, __uint_as_float(r[e + 1]) * f,
-                                    __uint_as_float(r[e + 2]) * f, __uint_as_float(r[e + 3]) * f);
+    {
+        // Split merge.  Every CTA counts itself in, aborted or not, so the
+        // per-(head, pair) counter is back at zero after every call.
+        if (p.splits > 1) {
+            // the last split of this (head, query pair) to finish merges all partials
+            __threadfence();
+            __syncthreads();
+            int* counter = p.counters + (size_t)h * (p.Tstride / 256) + pair;
+            if (tid == 0) *sLast = atomicAdd(counter, 1) == p.splits - 1;
+            __syncthreads();
+            if (*sLast) {
+                __threadfence();
+                const int rows = nq * 128;
+                for (int item = tid; item < rows * (D / 4); item += kAttendThreads) {
+                    const int rr = item / (D / 4), c4 = item % (D / 4);
+                    const int t = pair * 256 + rr;
+                    if (t >= p.T) continue;
+                    float M = -INFINITY;
+                    for (int s = 0; s < p.splits; ++s)
+                        M = fmaxf(M, __ldcg(p.part_ml + (((size_t)s * p.H + h) * p.Tstride + t) * 2));
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    float lsum = 0.f;
+                    for (int s = 0; s < p.splits; ++s) {
+                        const size_t pr = ((size_t)s * p.H + h) * p.Tstride + t;
+                        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + pr * 2));
+                        const float w = ex2_approx(ml.x - M);
+                        lsum += w * ml.y;
+                        const float4 o = __ldcg(reinterpret_cast<const float4*>(p.part_o + pr * D + c4 * 4));
+                        acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
+                    }
+                    const float inv = 1.f / lsum;
+                    *reinterpret_cast<float4*>(p.out + ((size_t)t * p.H + h) * D + c4 * 4) =
+                        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                }
+                if (tid == 0) *counter = 0;
             }
         }
-        if (store && !direct) *reinterpret_cast<float2*>(p.part_ml + prow_i * 2) = make_float2(m_run * a, l_run);
-    }
-    if (aborted && tid == 0) {
-        // drain: every MMA this thread issued, then every TMA copy still in flight
-        mma_commit(&bars[kBarDrain]);
-        mbar_wait(&bars[kBarDrain], 0, p.timeout_ns);
-        if (q_pending) mbar_wait(&bars[kBarQ], 0, p.timeout_ns);
-        for (int st = 0; st < 2; ++st)
-            while (consumed[st] < issued[st]) {
-                mbar_wait(&bars[kBarKV0 + st], (uint32_t)(consumed[st] & 1), p.timeout_ns);
-                consumed[st]++;
-            }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, 512);
     }
 }
 
@@ -402,53 +587,18 @@ size_t attend_smem_bytes(int d) {
 }
 
 cudaError_t launch_attend(const AttendParams& p, const AttendMaps& maps, cudaStream_t s) {
-    const int grid = p.H * p.qtiles * p.splits;
+    const int grid = p.H * p.npairs * p.splits;
     if (p.d == 128) {
         const int smem = AttendSmem<128>::kAlloc;
         cudaError_t e = cudaFuncSetAttribute(attend_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        attend_kernel<128><<<grid, 128, smem, s>>>(p, maps);
+        attend_kernel<128><<<grid, kAttendThreads, smem, s>>>(p, maps);
     } else {
         const int smem = AttendSmem<64>::kAlloc;
         cudaError_t e = cudaFuncSetAttribute(attend_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        attend_kernel<64><<<grid, 128, smem, s>>>(p, maps);
+        attend_kernel<64><<<grid, kAttendThreads, smem, s>>>(p, maps);
     }
-    return cudaGetLastError();
-}
-
-// ============================================================== K5: combine splits
-// O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s, with M = max_s m_s (log2 units).
-__global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ CombineParams p) {
-    const int d = p.d;
-    const int tpr = d / 4;                        // threads per row, float4 each
-    const int rows_per_block = 128 / tpr;
-    const int row = blockIdx.x * rows_per_block + threadIdx.x / tpr;   // over T * H, token-major
-    const int c = threadIdx.x % tpr;
-    if (row >= p.T * p.H) return;
-    const int t = row / p.H, h = row % p.H;
-    float M = -INFINITY;
-    for (int s = 0; s < p.splits; ++s)
-        M = fmaxf(M, p.part_ml[(((size_t)s * p.H + h) * p.Tstride + t) * 2]);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float lsum = 0.f;
-    for (int s = 0; s < p.splits; ++s) {
-        const size_t pr = ((size_t)s * p.H + h) * p.Tstride + t;
-        const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + pr * 2);
-        const float w = ex2_approx(ml.x - M);
-        lsum += w * ml.y;
-        const float4 o = *reinterpret_cast<const float4*>(p.part_o + pr * d + c * 4);
-        acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
-    }
-    const float inv = 1.f / lsum;
-    *reinterpret_cast<float4*>(p.out + ((size_t)t * p.H + h) * d + c * 4) =
-        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-}
-
-cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
-    const int rows_per_block = 128 / (p.d / 4);
-    const int rows = p.T * p.H;
-    combine_kernel<<<(rows + rows_per_block - 1) / rows_per_block, 128, 0, s>>>(p);
     return cudaGetLastError();
 }
 

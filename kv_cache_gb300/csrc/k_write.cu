@@ -12,13 +12,15 @@
 // K|V).  The chunk's slots are cut into 16-slot groups aligned in the ring
 // (the V ring is slot-contiguous, so a group is one 16-byte store per head_dim
 // row); the groups are dealt to the cluster's CTAs in ring order.  Each CTA
-// stages its rows in shared memory, takes its local amax, the cluster reduces
-// the amax through distributed shared memory, and each CTA quantises its rows
-// from shared memory.  Input bytes are read once.
+// pulls its rows (and, for K, their RoPE table rows) into shared memory with
+// bulk TMA copies issued by the 32 lanes of warp 0, takes its local amax, the
+// cluster reduces the amax through distributed shared memory, and each CTA
+// quantises its rows from shared memory.  Input bytes are read once.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "kvring_internal.h"
+#include "tc.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -38,10 +40,23 @@ __device__ __forceinline__ int group_slot_token(const WriteParams& p, int k, int
     return t < p.T ? t : -1;
 }
 
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx_only(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __global__ void __launch_bounds__(kWriteThreads) write_kernel(const __grid_constant__ WriteParams p) {
-    extern __shared__ __align__(16) uint8_t smem[];
+    extern __shared__ __align__(128) uint8_t smem[];
     __shared__ float s_red[kWriteThreads / 32];
     __shared__ float s_amax;
+    __shared__ __align__(8) uint64_t s_bar;
 
     cg::cluster_group cluster = cg::this_cluster();
     const int CL = (int)cluster.num_blocks();
@@ -53,28 +68,67 @@ __global__ void __launch_bounds__(kWriteThreads) write_kernel(const __grid_const
     const int k0 = rank * p.groups / CL;
     const int k1 = (rank + 1) * p.groups / CL;
     const int nloc = (k1 - k0) * 16;
-    uint16_t* sx = reinterpret_cast<uint16_t*>(smem);     // [nloc][d] bf16
+    uint16_t* sx = reinterpret_cast<uint16_t*>(smem);                              // [nloc][d] bf16
+    float2* stab = reinterpret_cast<float2*>(smem + (size_t)nloc * d * 2);          // [nloc][d/2] (K only)
 
-    // ---- 1. stage rows, local amax (K: largest pair norm of the un-rotated pairs; V: largest |v|)
+    // ---- 1. bulk copies of this CTA's rows (and, for K, their RoPE table rows) into shared memory
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_bar)) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
     const uint16_t* src = is_v ? p.v : p.k;
-    const int vec_per_row = d / 8;
-    float local = 0.f;
-#pragma unroll 4
-    for (int q = tid; q < nloc * vec_per_row; q += kWriteThreads) {
-        const int li = q / vec_per_row, c = q - li * vec_per_row;
-        int slot;
-        const int t = group_slot_token(p, k0 + li / 16, li % 16, slot);
-        uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if (t >= 0) {
-            w = __ldg(reinterpret_cast<const uint4*>(src + ((size_t)t * p.H + h) * d + c * 8));
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float x0 = bf16_lo(ws[e]), x1 = bf16_hi(ws[e]);
-                local = is_v ? fmaxf(local, fmaxf(fabsf(x0), fabsf(x1))) : fmaxf(local, pair_norm(x0, x1));
+    if (tid < 32) {
+        uint32_t bytes = 0;
+        for (int li = tid; li < nloc; li += 32) {
+            int slot;
+            if (group_slot_token(p, k0 + li / 16, li % 16, slot) >= 0) bytes += is_v ? 2 * d : 6 * d;
+        }
+        if (bytes) mbar_expect_tx_only(&s_bar, bytes);
+        __syncwarp();
+        for (int li = tid; li < nloc; li += 32) {
+            int slot;
+            const int t = group_slot_token(p, k0 + li / 16, li % 16, slot);
+            if (t < 0) continue;
+            bulk_g2s(sx + (size_t)li * d, src + ((size_t)t * p.H + h) * d, 2 * d, &s_bar);
+            if (!is_v) bulk_g2s(stab + (size_t)li * (d / 2), p.rope + (size_t)(p.pos0 + t) * (d / 2), 4 * d, &s_bar);
+        }
+        __syncwarp();
+        if (tid == 0) mbar_arrive1(&s_bar);
+    }
+    // bounded wait for the copies (2 s), then once more before giving up on them
+    {
+        uint32_t done = 0;
+        for (int round = 0; round < 2 && !done; ++round) {
+            const uint64_t t0 = globaltimer_ns();
+            while (true) {
+                asm volatile(
+                    "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                    : "=r"(done) : "r"(smem_u32(&s_bar)) : "memory");
+                if (done || globaltimer_ns() - t0 > 2000000000ull) break;
+            }
+            if (!done && tid == 0 && atomicCAS(p.err, 0, KVRING_ETIMEOUT) == 0) {
+                p.err[1] = kKernelWrite;
+                p.err[2] = 1;
+                p.err[3] = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
             }
         }
-        *reinterpret_cast<uint4*>(sx + (size_t)li * d + c * 8) = w;
+    }
+
+    // ---- 2. local amax (K: largest pair norm of the un-rotated pairs; V: largest |v|)
+    const int vec_per_row = d / 8;
+    float local = 0.f;
+    for (int qq = tid; qq < nloc * vec_per_row; qq += kWriteThreads) {
+        const int li = qq / vec_per_row, c = qq - li * vec_per_row;
+        int slot;
+        if (group_slot_token(p, k0 + li / 16, li % 16, slot) < 0) continue;
+        const uint4 w = *reinterpret_cast<const uint4*>(sx + (size_t)li * d + c * 8);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float x0 = bf16_lo(ws[e]), x1 = bf16_hi(ws[e]);
+            local = is_v ? fmaxf(local, fmaxf(fabsf(x0), fabsf(x1))) : fmaxf(local, pair_norm(x0, x1));
+        }
     }
 #pragma unroll
     for (int off = 16; off; off >>= 1) local = fmaxf(local, __shfl_xor_sync(0xffffffffu, local, off));
@@ -85,28 +139,27 @@ __global__ void __launch_bounds__(kWriteThreads) write_kernel(const __grid_const
         for (int w = 0; w < kWriteThreads / 32; ++w) m = fmaxf(m, s_red[w]);
         s_amax = m;
     }
-    // ---- 2. chunk amax over the cluster (distributed shared memory)
+    // ---- 3. chunk amax over the cluster (distributed shared memory)
     cluster.sync();
     float amax = 0.f;
     for (int r = 0; r < CL; ++r) amax = fmaxf(amax, *cluster.map_shared_rank(&s_amax, r));
     const float inv = inv_of(amax);
 
-    // ---- 3. quantise and store
+    // ---- 4. quantise and store
     if (!is_v) {
         const int c16n = d / 16;
-        for (int q = tid; q < nloc * c16n; q += kWriteThreads) {
-            const int li = q / c16n, c = q - li * c16n;
+        for (int qq = tid; qq < nloc * c16n; qq += kWriteThreads) {
+            const int li = qq / c16n, c = qq - li * c16n;
             int slot;
-            const int t = group_slot_token(p, k0 + li / 16, li % 16, slot);
-            if (t < 0) continue;
+            if (group_slot_token(p, k0 + li / 16, li % 16, slot) < 0) continue;
             const uint4* xs = reinterpret_cast<const uint4*>(sx + (size_t)li * d + c * 16);
             const uint4 a = xs[0], b = xs[1];
             const uint32_t ws[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            const float4* tab = reinterpret_cast<const float4*>(p.rope + (size_t)(p.pos0 + t) * (d / 2) + c * 8);
-            uint32_t out[4] = {0u, 0u, 0u, 0u};
+            const float4* tab = reinterpret_cast<const float4*>(stab + (size_t)li * (d / 2) + c * 8);
+            uint32_t out[4];
 #pragma unroll
             for (int e2 = 0; e2 < 4; ++e2) {
-                const float4 cs = __ldg(tab + e2);          // pairs 2*e2 and 2*e2+1
+                const float4 cs = tab[e2];          // pairs 2*e2 and 2*e2+1
                 float y0, y1, z0, z1;
                 rope_pair(bf16_lo(ws[2 * e2]), bf16_hi(ws[2 * e2]), cs.x, cs.y, y0, y1);
                 rope_pair(bf16_lo(ws[2 * e2 + 1]), bf16_hi(ws[2 * e2 + 1]), cs.z, cs.w, z0, z1);
@@ -118,8 +171,8 @@ __global__ void __launch_bounds__(kWriteThreads) write_kernel(const __grid_const
         }
     } else {
         const int ng = k1 - k0;
-        for (int q = tid; q < d * ng; q += kWriteThreads) {
-            const int kk = q / d, dd = q - kk * d;
+        for (int qq = tid; qq < d * ng; qq += kWriteThreads) {
+            const int kk = qq / d, dd = qq - kk * d;
             uint32_t words[4] = {0u, 0u, 0u, 0u};
             uint32_t written = 0;    // bit j: slot j of the group belongs to this chunk
             int slot0 = 0;
@@ -158,7 +211,7 @@ __global__ void __launch_bounds__(kWriteThreads) write_kernel(const __grid_const
 cudaError_t launch_write(const WriteParams& p, cudaStream_t s) {
     const int CL = p.groups < 8 ? p.groups : 8;
     const int per = (p.groups + CL - 1) / CL;
-    const size_t smem = (size_t)per * 16 * p.d * sizeof(uint16_t);
+    const size_t smem = (size_t)per * 16 * p.d * (sizeof(uint16_t) + 2 * sizeof(float));   // rows + table rows
     cudaError_t e = cudaFuncSetAttribute(write_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

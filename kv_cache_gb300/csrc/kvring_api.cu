@@ -37,7 +37,7 @@ int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 struct kvring {
     kvring_config cfg{};
     bool host_only = false;
-    int device = 0, num_sms = 0, attend_ctas_per_sm = 1;
+    int device = 0, num_sms = 0;
     int64_t Rpad = 0, Tstride = 0;
     int max_splits = 1;
     int64_t resets = 0;
@@ -52,6 +52,7 @@ struct kvring {
     float* qamax = nullptr;     // [H][Tstride]
     float* part_o = nullptr;    // [max_splits][H][Tstride][d]
     float* part_ml = nullptr;   // [max_splits][H][Tstride][2]
+    int* counters = nullptr;    // [H][Tstride/256] split arrivals per (head, query pair)
     int* err = nullptr;         // [4]
     AttendMaps maps{};
     // testing aid
@@ -73,12 +74,13 @@ int cuda_fail(kvring_t* r, cudaError_t e, const char* what) {
 }
 
 void free_device(kvring_t* r) {
-    void* ptrs[] = {r->k8, r->vt8, r->kamax, r->vamax, r->rope, r->q8, r->qamax, r->part_o, r->part_ml, r->err};
+    void* ptrs[] = {r->k8, r->vt8, r->kamax, r->vamax, r->rope, r->q8, r->qamax, r->part_o, r->part_ml, r->counters, r->err};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     r->k8 = r->vt8 = r->q8 = nullptr;
     r->kamax = r->vamax = r->qamax = r->part_o = r->part_ml = nullptr;
     r->rope = nullptr;
+    r->counters = nullptr;
     r->err = nullptr;
 }
 
@@ -128,8 +130,8 @@ int check_config(const kvring_config* c) {
     if (c->num_heads < 1 || c->num_heads > 256) return fail(nullptr, KVRING_EINVAL, "num_heads out of range [1, 256]");
     if (c->head_dim != 64 && c->head_dim != 128) return fail(nullptr, KVRING_EINVAL, "head_dim must be 64 or 128");
     if (c->capacity < 1 || c->capacity > (1 << 20)) return fail(nullptr, KVRING_EINVAL, "capacity out of range [1, 2^20]");
-    if (c->max_tokens_per_write < 1 || c->max_tokens_per_write > c->capacity || c->max_tokens_per_write > 4096)
-        return fail(nullptr, KVRING_EINVAL, "max_tokens_per_write out of range [1, min(capacity, 4096)]");
+    if (c->max_tokens_per_write < 1 || c->max_tokens_per_write > c->capacity || c->max_tokens_per_write > 2048)
+        return fail(nullptr, KVRING_EINVAL, "max_tokens_per_write out of range [1, min(capacity, 2048)]");
     if (c->max_position < 0) return fail(nullptr, KVRING_EINVAL, "max_position must be >= 0");
     if (c->rope_theta < 0 || !std::isfinite(c->rope_theta)) return fail(nullptr, KVRING_EINVAL, "rope_theta must be finite and >= 0");
     if (c->flags & ~KVRING_FLAG_HOST_ONLY) return fail(nullptr, KVRING_EINVAL, "unknown flag bits");
@@ -139,7 +141,7 @@ int check_config(const kvring_config* c) {
 int choose_splits(const kvring_t* r, int units, int ntiles) {
     int best = 1;
     long long best_cost = -1;
-    const long long slots = (long long)r->num_sms * r->attend_ctas_per_sm;
+    const long long slots = (long long)r->num_sms;   // one attention CTA per SM
     for (int s = 1; s <= std::min(r->max_splits, ntiles); ++s) {
         const int tps = (ntiles + s - 1) / s;
         const int se = (ntiles + tps - 1) / tps;
@@ -170,7 +172,7 @@ int kvring_create(const kvring_config* cfg_in, kvring_t** out) {
     r->cfg = cfg;
     r->host_only = (cfg.flags & KVRING_FLAG_HOST_ONLY) != 0;
     r->Rpad = round_up(cfg.capacity, 128);
-    r->Tstride = round_up(cfg.max_tokens_per_write, 128);
+    r->Tstride = round_up(cfg.max_tokens_per_write, 256);
     r->layers.resize(cfg.num_layers);
     for (auto& l : r->layers) {
         l.pos.assign(cfg.capacity, -1);
@@ -189,8 +191,8 @@ int kvring_create(const kvring_config* cfg_in, kvring_t** out) {
     r->num_sms = prop.multiProcessorCount;
 
     const int64_t L = cfg.num_layers, H = cfg.num_heads, d = cfg.head_dim;
-    const int64_t ntiles_max = r->Rpad / 128, qtiles_max = r->Tstride / 128;
-    r->max_splits = (int)std::max<int64_t>(1, std::min<int64_t>(ntiles_max, (4 * r->num_sms + H * qtiles_max - 1) / (H * qtiles_max)));
+    const int64_t ntiles_max = r->Rpad / 128, npairs_max = r->Tstride / 256;
+    r->max_splits = (int)std::max<int64_t>(1, std::min<int64_t>(ntiles_max, (4 * r->num_sms + H * npairs_max - 1) / (H * npairs_max)));
     const size_t ring_bytes = (size_t)(L * H * r->Rpad * d);
     const size_t amax_bytes = (size_t)(L * H * r->Rpad) * sizeof(float);
     const size_t rope_bytes = (size_t)cfg.max_position * (d / 2) * sizeof(float2);
@@ -201,6 +203,7 @@ int kvring_create(const kvring_config* cfg_in, kvring_t** out) {
         {(void**)&r->q8, (size_t)(H * r->Tstride * d)}, {(void**)&r->qamax, (size_t)(H * r->Tstride) * sizeof(float)},
         {(void**)&r->part_o, (size_t)(r->max_splits * H * r->Tstride * d) * sizeof(float)},
         {(void**)&r->part_ml, (size_t)(r->max_splits * H * r->Tstride * 2) * sizeof(float)},
+        {(void**)&r->counters, (size_t)(H * npairs_max) * sizeof(int)},
         {(void**)&r->err, 4 * sizeof(int)},
     };
     for (auto& a : allocs) {
@@ -235,7 +238,6 @@ int kvring_create(const kvring_config* cfg_in, kvring_t** out) {
             return rc;
         }
     }
-    r->attend_ctas_per_sm = attend_smem_bytes((int)d) * 2 + 2048 <= (size_t)prop.sharedMemPerMultiprocessor ? 2 : 1;
     *out = r;
     return KVRING_OK;
 }
@@ -288,6 +290,7 @@ int kvring_write(kvring_t* r, int32_t layer, const void* k, const void* v, int32
             groups = (int)std::min<int64_t>(p.ngroups_ring, g1 + g2);
         }
         p.groups = groups;
+        p.err = r->err;
         cudaError_t e = launch_write(p, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(r, e, "write kernel launch");
         r->launches += 1;
@@ -344,6 +347,7 @@ int kvring_attend(kvring_t* r, int32_t layer, const void* q, int32_t n_q, float*
     ap.out = out;
     ap.part_o = r->part_o;
     ap.part_ml = r->part_ml;
+    ap.counters = r->counters;
     ap.err = r->err;
     ap.T = n_q;
     ap.H = H;
@@ -352,9 +356,9 @@ int kvring_attend(kvring_t* r, int32_t layer, const void* q, int32_t n_q, float*
     ap.Tstride = (int)r->Tstride;
     ap.count = (int)L.count;
     ap.layer = layer;
-    ap.qtiles = Tpad / 128;
+    ap.npairs = (n_q + 255) / 256;
     ap.ntiles = (int)((L.count + 127) / 128);
-    ap.splits = choose_splits(r, H * ap.qtiles, ap.ntiles);
+    ap.splits = choose_splits(r, H * ap.npairs, ap.ntiles);
     ap.tiles_per_split = (ap.ntiles + ap.splits - 1) / ap.splits;
     ap.splits = (ap.ntiles + ap.tiles_per_split - 1) / ap.tiles_per_split;
     ap.log2e_rsqrt_d = (float)(1.4426950408889634 / std::sqrt((double)d));
@@ -365,20 +369,6 @@ int kvring_attend(kvring_t* r, int32_t layer, const void* q, int32_t n_q, float*
     e = launch_attend(ap, r->maps, s);
     if (e != cudaSuccess) return cuda_fail(r, e, "attention kernel launch");
     r->launches += 1;
-    if (ap.splits > 1) {
-        CombineParams cp{};
-        cp.part_o = r->part_o;
-        cp.part_ml = r->part_ml;
-        cp.out = out;
-        cp.T = n_q;
-        cp.H = H;
-        cp.d = d;
-        cp.Tstride = (int)r->Tstride;
-        cp.splits = ap.splits;
-        e = launch_combine(cp, s);
-        if (e != cudaSuccess) return cuda_fail(r, e, "combine kernel launch");
-        r->launches += 1;
-    }
     return KVRING_OK;
 }
 
@@ -476,11 +466,16 @@ int kvring_check_device(kvring_t* r, void* stream) {
     if (e == cudaSuccess) e = cudaMemcpy(w, r->err, sizeof(w), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(r, e, "reading the device error word");
     if (w[0] == 0) return KVRING_OK;
-    static const char* sites[] = {"?", "Q tile", "K/V tile", "S = QK^T", "O += PV", "final O"};
-    const int site = (w[2] >= 0 && w[2] <= 5) ? w[2] : 0;
-    r->error = std::string("device wait timed out in the attention kernel (wait for ") + sites[site] +
-               ", block " + std::to_string(w[3]) + ")";
+    static const char* sites[] = {"?", "Q tiles", "K/V stage full", "K/V stage free", "S", "P", "O", "fp16 V full",
+                                  "fp16 V free"};
+    const int site = (w[2] >= 0 && w[2] <= 8) ? w[2] : 0;
+    const char* kernel = w[1] == 2 ? "write" : "attention";
+    r->error = std::string("device wait timed out in the ") + kernel + " kernel (wait for " +
+               (w[1] == 2 ? "input rows" : sites[site]) + ", block " + std::to_string(w[3]) + ")";
     e = cudaMemset(r->err, 0, sizeof(w));
+    // a CTA that gave up may have left a split counter behind
+    if (e == cudaSuccess)
+        e = cudaMemset(r->counters, 0, (size_t)r->cfg.num_heads * (r->Tstride / 256) * sizeof(int));
     if (e != cudaSuccess) return cuda_fail(r, e, "clearing the device error word");
     return KVRING_ETIMEOUT;
 }

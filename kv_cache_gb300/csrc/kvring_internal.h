@@ -14,7 +14,7 @@ constexpr float kE4M3Max = 448.0f;
 
 // Device error word: [0] = status (0 or KVRING_ETIMEOUT), [1] = kernel id,
 // [2] = wait site, [3] = block index that gave up.
-enum KernelId : int { kKernelAttend = 1 };
+enum KernelId : int { kKernelAttend = 1, kKernelWrite = 2 };
 
 // ---------------------------------------------------------------- write (K1)
 struct WriteParams {
@@ -31,6 +31,7 @@ struct WriteParams {
     int groups;               // 16-slot groups touched by the chunk
     int group0;               // first group in cyclic order
     int ngroups_ring;         // ceil(R / 16)
+    int* err;                 // device error word
 };
 cudaError_t launch_write(const WriteParams& p, cudaStream_t s);
 
@@ -57,20 +58,21 @@ struct QPrepParams {
 };
 cudaError_t launch_qprep(const QPrepParams& p, cudaStream_t s);
 
-// ---------------------------------------------------------------- attention (K4 + K5)
+// ---------------------------------------------------------------- attention (K4)
 struct AttendParams {
     const float* kamax;       // this layer [H][Rpad]
     const float* vamax;       // this layer [H][Rpad]
     const float* qamax;       // [H][Tstride]
-    float* out;               // fp32 [T][H][d]          (splits == 1)
+    float* out;               // fp32 [T][H][d]
     float* part_o;            // fp32 [splits][H][Tstride][d]   (splits > 1)
-    float* part_ml;           // fp32 [splits][H][Tstride][2]
+    float* part_ml;           // fp32 [splits][H][Tstride][2]   (splits > 1)
+    int* counters;            // [H][Tstride/256], zero between calls (splits > 1)
     int* err;                 // device error word
     int T, H, d, Rpad, Tstride;
     int count;                // valid slots
     int layer;
-    int qtiles;               // ceil(T / 128)
-    int splits;               // KV splits per (head, q tile)
+    int npairs;               // ceil(T / 256): pairs of 128-row query tiles
+    int splits;               // KV splits per (head, query pair)
     int tiles_per_split;
     int ntiles;               // ceil(count / 128)
     float log2e_rsqrt_d;      // log2(e) / sqrt(d)
@@ -83,14 +85,6 @@ struct AttendMaps {
     CUtensorMap vt8;          // 3-D {Rpad, d, L*H}
 };
 cudaError_t launch_attend(const AttendParams& p, const AttendMaps& maps, cudaStream_t s);
-
-struct CombineParams {
-    const float* part_o;
-    const float* part_ml;
-    float* out;
-    int T, H, d, Tstride, splits;
-};
-cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 
 size_t attend_smem_bytes(int d);
 
