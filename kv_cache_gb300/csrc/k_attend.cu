@@ -81,52 +81,68 @@ cudaError_t launch_qprep(const QPrepParams& p, cudaStream_t s) {
 }
 
 
+
 // ============================================================== K4: attention
 // One CTA of 14 warps per (head, pair of 128-row query tiles, KV split):
 //   warps 0-3   softmax for query tile 0 (tensor-memory lanes 0-127 of S0, O0)
 //   warps 4-7   softmax for query tile 1 (S1, O1)
-//   warps 8-11  widen each V tile from e4m3 to fp16 (exact)
-//   warp 12     TMA producer (Q tiles once, then K/V tiles through 2 stages)
-//   warp 13     tcgen05 issuer: S_q(j+1) = Q_q K_{j+1}^T goes out before
-//               O_q += P_q(j) V_j, so each softmax group finds its next S ready
+//   warps 8-11  per tile: per-slot scales into shared memory, then V e4m3 -> fp16
+//   warp 12     TMA producer (the query tiles once, then K/V tiles, 3 stages)
+//   warp 13     tcgen05 issuer
 // Tensor memory (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [384,384+d).
-// The two query tiles share every K/V tile, halving K/V shared-memory traffic
-// per FLOP.  Hand-offs are mbarriers; every wait is bounded and also gives up
-// as soon as another warp has recorded a time-out.
+// The softmax reads its S row once, writes P as packed fp16 back over the first
+// 64 columns of S, and O_q += P_q V runs with A in tensor memory.  The issuer
+// puts S_q(j+1) right behind O_q += P_q(j) V_j in the tensor pipe, so when a
+// softmax group sees S_q(j+1) its previous product is done: O_q can be rescaled
+// and P_q rewritten without another wait.  The two query tiles share every K/V
+// tile and alternate on the tensor pipe.  Hand-offs are mbarriers; every wait
+// is bounded and gives up as soon as another warp has recorded a time-out.
 template <int D>
 struct AttendSmem {
-    static constexpr int kStages = 2;
+    static constexpr int kStages = 3;
     static constexpr int kQ = 128 * D;            // one query tile, e4m3
     static constexpr int kK = 128 * D;            // K tile [128 slots][D], e4m3
     static constexpr int kV = D * 128;            // V tile [D][128 slots], e4m3
     static constexpr int kV16 = D * 128 * 2;      // V tile in fp16: 2 K-blocks of [D][64]
-    static constexpr int kP = 128 * 128 * 2;      // P in fp16: 2 K-blocks of [128][64]
+    static constexpr int kCol = 2 * 128 * 4 + 4 * 4 * 4;   // per-slot k scale, V ratio; 4 group records
     static constexpr int offQ = 0;
     static constexpr int offK = offQ + 2 * kQ;
     static constexpr int offV = offK + kStages * kK;
     static constexpr int offV16 = offV + kStages * kV;
-    static constexpr int offP = offV16 + 2 * kV16;
-    static constexpr int offBar = offP + 2 * kP;
-    static constexpr int kBars = 16;
+    static constexpr int offCol = offV16 + 2 * kV16;
+    static constexpr int offBar = offCol + 2 * kCol;
+    static constexpr int kBars = 20;
     static constexpr int offMisc = offBar + kBars * 8;
     static constexpr int kBytes = offMisc + 64;
     static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
+// Per-tile scale record written by the converter warps: for column c, the K scale
+// ks[c] and the V ratio rr[c] = (V scale) / (reference); for each 32-column group
+// g, whether all its columns are valid and share one (ks, rr), and then that
+// pair with 1/rr and log2(rr).
+struct ColInfo {
+    float ks[128];
+    float rr[128];
+    float gks[4], glg[4], gri[4];
+    int guni[4];
+};
+
 // mbarrier slots
 enum : int {
-    kBQ = 0,        // Q tiles landed (TMA)
-    kBKVF = 1,      // [2] K/V stage full (TMA)
-    kBKVE = 3,      // [2] K/V stage free: S MMAs done (commit) + 128 converter arrivals
-    kBSF = 5,       // [2] S_q computed (commit)
-    kBPF = 7,       // [2] P_q written and S_q read (128 softmax arrivals)
-    kBOF = 9,       // [2] O_q += P_q V done (commit)
-    kBVF = 11,      // [2] fp16 V buffer full (128 converter arrivals)
-    kBVE = 13,      // [2] fp16 V buffer free (commit after both PV MMAs)
-    kBDrain = 15,   // drain after an abort
+    kBQ = 0,        // query tiles landed (TMA)
+    kBKVF = 1,      // [3] K/V stage full (TMA)
+    kBKVE = 4,      // [3] K/V stage free: S MMAs done (commit) + 128 converter arrivals
+    kBSF = 7,       // [2] S_q computed (commit)
+    kBPF = 9,       // [2] P_q in tensor memory (128 softmax arrivals)
+    kBOF = 11,      // [2] O_q += P_q V done (commit)
+    kBVF = 13,      // [2] fp16 V buffer full (128 converter arrivals)
+    kBVE = 15,      // [2] fp16 V buffer and scale record free (commit after both PV MMAs)
+    kBCF = 17,      // [2] scale record of the tile written (128 converter arrivals)
+    kBDrain = 19,   // drain after an abort
 };
 enum : int { kWaitQ = 1, kWaitKVFull = 2, kWaitKVEmpty = 3, kWaitS = 4, kWaitP = 5, kWaitO = 6, kWaitV16Full = 7,
-             kWaitV16Empty = 8 };
+             kWaitV16Empty = 8, kWaitCol = 9 };
 constexpr int kAttendThreads = 448;
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -141,7 +157,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     int ok = 1;
     if ((threadIdx.x & 31) == 0) {
         if (!mbar_try_wait(bar, parity)) {
-            uint64_t t0 = globaltimer_ns();
+            const uint64_t t0 = globaltimer_ns();
             while (true) {
                 if (mbar_try_wait(bar, parity)) break;
                 if (*abort_flag) { ok = 0; break; }
@@ -169,14 +185,15 @@ __device__ __forceinline__ void issue_s(uint32_t tS, uint32_t aQ, uint32_t aK) {
         mma_f8(tS, make_sdesc(aQ + k * 32, D), make_sdesc(aK + k * 32, D), id, k > 0 ? 1u : 0u);
 }
 
+// O += P V for one 128-slot tile: P (fp16) in tensor memory at tP, 8 columns per
+// 16-slot step; V fp16 in shared memory, 2 K-blocks of [D][64].
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t aP, uint32_t aV16, bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t aV16, bool accumulate) {
     constexpr uint32_t id = make_idesc(128, D);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        const uint32_t offp = (k >> 2) * (128 * 128) + (k & 3) * 32;
         const uint32_t offv = (k >> 2) * (D * 128) + (k & 3) * 32;
-        mma_f16(tO, make_sdesc(aP + offp, 128), make_sdesc(aV16 + offv, 128), id, (accumulate || k > 0) ? 1u : 0u);
+        mma_f16_ts(tO, tP + k * 8, make_sdesc(aV16 + offv, 128), id, (accumulate || k > 0) ? 1u : 0u);
     }
 }
 
@@ -185,6 +202,8 @@ __device__ __forceinline__ float lg2_approx(float x) {
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
 template <int D>
 __global__ void __launch_bounds__(kAttendThreads, 1)
@@ -197,7 +216,7 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
     uint8_t* sK = smem + L::offK;
     uint8_t* sV = smem + L::offV;
     uint8_t* sV16 = smem + L::offV16;
-    uint8_t* sP = smem + L::offP;
+    ColInfo* sCol = reinterpret_cast<ColInfo*>(smem + L::offCol);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::offBar);
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + L::offMisc);
     volatile int* sAbort = reinterpret_cast<volatile int*>(smem + L::offMisc + 4);
@@ -222,13 +241,13 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
 
     if (warp == 0) tmem_alloc(sTmem, 512);
     if (tid == 0) {
-        const int counts[L::kBars] = {1, 1, 1, 129, 129, 1, 1, 128, 128, 1, 1, 128, 128, 1, 1, 1};
+        const int counts[L::kBars] = {1, 1, 1, 1, 129, 129, 129, 1, 1, 128, 128, 1, 1, 128, 128, 1, 1, 128, 128, 1};
         for (int b = 0; b < L::kBars; ++b) mbar_init(&bars[b], counts[b]);
         fence_mbar_init();
         *sAbort = 0;
         *sLast = 0;
     }
-    // V scale reference of this split: largest V scale among its valid slots (converter warps)
+    // V scale reference of this split: largest V scale among its valid slots
     if (warp >= 8 && warp < 12) {
         const int c = tid - 256;
         const int s_end = min((j0 + nt) * 128, p.count);
@@ -246,7 +265,7 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
     const float inv_sv_ref = __frcp_rn(sv_ref);
 
     // softmax state (warps 0-7), kept for the epilogue
-    const int q = warp >> 2;                     // query tile of a softmax warp
+    const int q = warp >> 2;
     const int wq = warp & 3;
     const int row = tid & 127;
     const int qrow = (2 * pair + q) * 128 + row;
@@ -257,131 +276,129 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
     for (int st = 0; st < NST; ++st) issued[st] = 0;
     bool q_issued = false;
 
+    // Register split: the launch gives every thread 128 registers (448 x 128 =
+    // 57,344); the 6 non-softmax warps drop to 64 and the 8 softmax warps take
+    // 168 (192 x 64 + 256 x 168 = 55,296), so the increase always fits.
+    if (warp < 8) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 168;" ::: "memory");
+    } else {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 64;" ::: "memory");
+    }
+
     if (warp < 8) {
         // ------------------------------------------------------------ softmax
         const bool active = q < nq;
-        const uint32_t tS = tmem + 128 * q;
-        const uint32_t tO = tmem + 256 + 128 * q;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t tS = tmem + 128 * q + lane_off;
+        const uint32_t tO = tmem + 256 + 128 * q + lane_off;
         a = scale_of(__ldg(p.qamax + (size_t)h * p.Tstride + qrow)) * p.log2e_rsqrt_d;
-        uint8_t* prow = sP + q * L::kP + row * 128;
         for (int it = 0; active && it < nt; ++it) {
-            const int j = j0 + it;
-            const int nvalid = min(128, p.count - j * 128);
-            // per-slot scales of this tile, four 32-column groups; lane e holds column 32g + e
-            float ksv[4], rv[4], KS[4], RR[4], RI[4];
-            bool uni[4];
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                const int col = g * 32 + lane;
-                const bool valid = col < nvalid;
-                ksv[g] = valid ? scale_of(__ldg(kam + j * 128 + col)) : 0.f;
-                rv[g] = valid ? __fmul_rn(scale_of(__ldg(vam + j * 128 + col)), inv_sv_ref) : 0.f;
-                KS[g] = __shfl_sync(0xffffffffu, ksv[g], 0);
-                RR[g] = __shfl_sync(0xffffffffu, rv[g], 0);
-                uni[g] = __all_sync(0xffffffffu, valid && ksv[g] == KS[g] && rv[g] == RR[g]);
-                RI[g] = uni[g] ? __frcp_rn(RR[g]) : 0.f;
-            }
+            const int b = it & 1;
+            const int nvalid = min(128, p.count - (j0 + it) * 128);
+            if (!warp_wait(&bars[kBCF + b], (uint32_t)((it >> 1) & 1), sAbort, p, kWaitCol)) break;
+            const ColInfo& ci = sCol[b];
             if (!warp_wait(&bars[kBSF + q], (uint32_t)(it & 1), sAbort, p, kWaitS)) break;
             tc_fence_after();
-            // pass 1: row max of raw * k_scale
-            float tm = -INFINITY;
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                uint32_t r[32];
-                tmem_ld32(tS + lane_off + g * 32, r);
-                if (uni[g]) {
-                    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        m0 = fmaxf(m0, __uint_as_float(r[e]));
-                        m1 = fmaxf(m1, __uint_as_float(r[e + 1]));
-                        m2 = fmaxf(m2, __uint_as_float(r[e + 2]));
-                        m3 = fmaxf(m3, __uint_as_float(r[e + 3]));
-                    }
-                    tm = fmaxf(tm, fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * KS[g]);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float ks = __shfl_sync(0xffffffffu, ksv[g], e);
-                        if (g * 32 + e < nvalid) tm = fmaxf(tm, __uint_as_float(r[e]) * ks);
-                    }
-                }
-            }
-            // P_q buffer and O_q are free once O_q += P_q(j-1) V has finished
-            if (it > 0) {
-                if (!warp_wait(&bars[kBOF + q], (uint32_t)((it - 1) & 1), sAbort, p, kWaitO)) break;
-                tc_fence_after();
-            }
-            // lazy rescale: move the running max only when it grows by more than 2^8
-            const bool first = m_run == -INFINITY;
-            const bool grow = !first && (tm - m_run) * a > 8.f;
-            if (__any_sync(0xffffffffu, grow)) {
-                const float alpha = grow ? ex2_approx((m_run - tm) * a) : 1.f;
-#pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t r[32];
-                    tmem_ld32(tO + lane_off + cc * 32, r);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                    tmem_st32(tO + lane_off + cc * 32, r);
-                }
-                tmem_wait_st();
-                l_run *= alpha;
-            }
-            if (first || grow) m_run = tm;
-            const float ma = m_run * a;
-            // pass 2: P = 2^(x - m) * (V scale / reference), fp16, into shared memory.
-            // The row sum uses the rounded P (over the V ratio), the same weights the
-            // P V product sees, so the rounding of a dominant weight cancels.
             float lsum = 0.f;
+            uint32_t r[32], rn[32];
+            tmem_ld32(tS, r);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-                uint32_t r[32];
-                tmem_ld32(tS + lane_off + g * 32, r);
+                if (g < 3) tmem_ld32_async(tS + (g + 1) * 32, rn);
+                const bool uni = ci.guni[g] != 0;
+                // group max of raw * k_scale
+                float gm;
+                if (uni) {
+                    float m0 = fmax3(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]));
+                    float m1 = fmax3(__uint_as_float(r[3]), __uint_as_float(r[4]), __uint_as_float(r[5]));
+#pragma unroll
+                    for (int e = 6; e < 30; e += 4) {
+                        m0 = fmax3(m0, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+                        m1 = fmax3(m1, __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+                    }
+                    gm = fmax3(m0, m1, fmaxf(__uint_as_float(r[30]), __uint_as_float(r[31]))) * ci.gks[g];
+                } else {
+                    gm = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (g * 32 + e < nvalid) gm = fmaxf(gm, __uint_as_float(r[e]) * ci.ks[g * 32 + e]);
+                }
+                // lazy running max: moved only when it grows by more than 2^8; then O,
+                // the sums and this tile's P so far are rescaled (all warp-collective)
+                const bool first = m_run == -INFINITY;
+                const bool grow = !first && gm != -INFINITY && (gm - m_run) * a > 8.f;
+                if (__any_sync(0xffffffffu, grow)) {
+                    const float alpha = grow ? ex2_approx((m_run - gm) * a) : 1.f;
+                    tmem_wait_st();
+                    if (it > 0) {
+#pragma unroll
+                        for (int cc = 0; cc < D / 32; ++cc) {
+                            uint32_t o[32];
+                            tmem_ld32(tO + cc * 32, o);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tmem_st32(tO + cc * 32, o);
+                        }
+                    }
+                    const __half2 a2 = __float2half2_rn(alpha);
+                    for (int pg = 0; pg < g; ++pg) {
+                        uint32_t pp[16];
+                        tmem_ld16(tS + pg * 16, pp);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            uint32_t w = pp[e];
+                            __half2 hv = *reinterpret_cast<__half2*>(&w);
+                            hv = __hmul2(hv, a2);
+                            pp[e] = h2_bits(hv);
+                        }
+                        tmem_st16(tS + pg * 16, pp);
+                    }
+                    tmem_wait_st();
+                    l_run *= alpha;
+                    lsum *= alpha;
+                }
+                if (first || grow) m_run = gm;
+                const float ma = m_run * a;
+                // P = 2^(x - m) * (V scale ratio) as fp16; the row sum adds the rounded P
+                // over the ratio, the same weights that O += P V sees.
                 uint32_t pk[16];
-                if (uni[g]) {
-                    const float c1 = KS[g] * a;
-                    const float c0 = lg2_approx(RR[g]) - ma;
-                    float lg0 = 0.f, lg1 = 0.f;
+                if (uni) {
+                    const float c1 = ci.gks[g] * a;
+                    const float c0 = ci.glg[g] - ma;
+                    const float2 c1v = make_float2(c1, c1), c0v = make_float2(c0, c0);
+                    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const float p0 = ex2_approx(fmaf(__uint_as_float(r[e]), c1, c0));
-                        const float p1 = ex2_approx(fmaf(__uint_as_float(r[e + 1]), c1, c0));
-                        const __half2 hv = __floats2half2_rn(p0, p1);
-                        pk[e / 2] = *reinterpret_cast<const uint32_t*>(&hv);
-                        const float2 back = __half22float2(hv);
-                        lg0 += back.x;
-                        lg1 += back.y;
+                        const float2 x = ffma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c1v, c0v);
+                        const __half2 hv = __floats2half2_rn(ex2_approx(x.x), ex2_approx(x.y));
+                        pk[e / 2] = h2_bits(hv);
+                        acc = fadd2(acc, __half22float2(hv));
                     }
-                    lsum += (lg0 + lg1) * RI[g];
+                    lsum += (acc.x + acc.y) * ci.gri[g];
                 } else {
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const float ks0 = __shfl_sync(0xffffffffu, ksv[g], e);
-                        const float ks1 = __shfl_sync(0xffffffffu, ksv[g], e + 1);
-                        const float r0 = __shfl_sync(0xffffffffu, rv[g], e);
-                        const float r1 = __shfl_sync(0xffffffffu, rv[g], e + 1);
-                        const bool v0 = g * 32 + e < nvalid, v1 = g * 32 + e + 1 < nvalid;
-                        const float p0 = v0 ? ex2_approx(fmaf(__uint_as_float(r[e]) * ks0, a, -ma)) * r0 : 0.f;
-                        const float p1 = v1 ? ex2_approx(fmaf(__uint_as_float(r[e + 1]) * ks1, a, -ma)) * r1 : 0.f;
+                        const int c = g * 32 + e;
+                        const bool v0 = c < nvalid, v1 = c + 1 < nvalid;
+                        const float r0 = ci.rr[c], r1 = ci.rr[c + 1];
+                        const float p0 = v0 ? ex2_approx(fmaf(__uint_as_float(r[e]) * ci.ks[c], a, -ma)) * r0 : 0.f;
+                        const float p1 = v1 ? ex2_approx(fmaf(__uint_as_float(r[e + 1]) * ci.ks[c + 1], a, -ma)) * r1 : 0.f;
                         const __half2 hv = __floats2half2_rn(p0, p1);
-                        pk[e / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+                        pk[e / 2] = h2_bits(hv);
                         const float2 back = __half22float2(hv);
                         if (v0) lsum += __fdiv_rn(back.x, r0);
                         if (v1) lsum += __fdiv_rn(back.y, r1);
                     }
                 }
-                uint8_t* blk = prow + (g >> 1) * (128 * 128);
+                tmem_st16(tS + g * 16, pk);     // P group g -> columns [16g, 16g + 16) of S_q
+                if (g < 3) {
+                    tmem_wait_ld_dep(rn);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int cb = (g & 1) * 4 + c;
-                    *reinterpret_cast<uint4*>(blk + ((cb ^ (row & 7)) << 4)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                    for (int e = 0; e < 32; ++e) r[e] = rn[e];
                 }
             }
             l_run += lsum;
-            fence_proxy_async_smem();
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&bars[kBPF + q]);
         }
@@ -389,12 +406,33 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
             if (warp_wait(&bars[kBOF + q], (uint32_t)((nt - 1) & 1), sAbort, p, kWaitO)) tc_fence_after();
         }
     } else if (warp < 12) {
-        // ------------------------------------------------------------ V e4m3 -> fp16
+        // ------------------------------------------------------------ scales, then V e4m3 -> fp16
         const int c0 = tid - 256;
+        const int cw = warp - 8;
         for (int it = 0; it < nt; ++it) {
             const int st = it % NST, b = it & 1;
+            if (it >= 2 && !warp_wait(&bars[kBVE + b], (uint32_t)(((it >> 1) - 1) & 1), sAbort, p, kWaitV16Empty))
+                break;
+            {
+                const int s = (j0 + it) * 128 + c0;
+                const bool valid = s < p.count;
+                const float ks = valid ? scale_of(__ldg(kam + s)) : 0.f;
+                const float rr = valid ? __fmul_rn(scale_of(__ldg(vam + s)), inv_sv_ref) : 0.f;
+                ColInfo& ci = sCol[b];
+                ci.ks[c0] = ks;
+                ci.rr[c0] = rr;
+                const float KS = __shfl_sync(0xffffffffu, ks, 0);
+                const float RR = __shfl_sync(0xffffffffu, rr, 0);
+                const bool uni = __all_sync(0xffffffffu, valid && ks == KS && rr == RR);
+                if (lane == 0) {
+                    ci.gks[cw] = KS;
+                    ci.glg[cw] = uni ? lg2_approx(RR) : 0.f;
+                    ci.gri[cw] = uni ? __frcp_rn(RR) : 0.f;
+                    ci.guni[cw] = uni ? 1 : 0;
+                }
+                mbar_arrive(&bars[kBCF + b]);
+            }
             if (!warp_wait(&bars[kBKVF + st], (uint32_t)((it / NST) & 1), sAbort, p, kWaitKVFull)) break;
-            if (it >= 2 && !warp_wait(&bars[kBVE + b], (uint32_t)(((it >> 1) - 1) & 1), sAbort, p, kWaitV16Empty)) break;
             const uint8_t* src = sV + st * L::kV;
             uint8_t* dst = sV16 + b * L::kV16;
 #pragma unroll
@@ -447,7 +485,6 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
         // ------------------------------------------------------------ MMA issuer
         const uint32_t aQ = smem_u32(sQ);
         const uint32_t aK = smem_u32(sK);
-        const uint32_t aP = smem_u32(sP);
         const uint32_t aV16 = smem_u32(sV16);
         bool ok = warp_wait(&bars[kBQ], 0, sAbort, p, kWaitQ) && warp_wait(&bars[kBKVF], 0, sAbort, p, kWaitKVFull);
         if (ok) {
@@ -463,10 +500,16 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
         }
         for (int it = 0; ok && it < nt; ++it) {
             const int stn = (it + 1) % NST, b = it & 1;
+            ok = warp_wait(&bars[kBVF + b], (uint32_t)((it >> 1) & 1), sAbort, p, kWaitV16Full);
             for (int qq = 0; qq < nq && ok; ++qq) {
                 ok = warp_wait(&bars[kBPF + qq], (uint32_t)(it & 1), sAbort, p, kWaitP);
                 if (!ok) break;
                 tc_fence_after();
+                if (lane == 0) {
+                    issue_pv<D>(tmem + 256 + 128 * qq, tmem + 128 * qq, aV16 + b * L::kV16, it > 0);
+                    mma_commit(&bars[kBOF + qq]);
+                }
+                __syncwarp();
                 if (it + 1 < nt) {
                     if (qq == 0) {
                         ok = warp_wait(&bars[kBKVF + stn], (uint32_t)(((it + 1) / NST) & 1), sAbort, p, kWaitKVFull);
@@ -480,19 +523,17 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                     }
                     __syncwarp();
                 }
-                if (qq == 0) {
-                    ok = warp_wait(&bars[kBVF + b], (uint32_t)((it >> 1) & 1), sAbort, p, kWaitV16Full);
-                    if (!ok) break;
-                    tc_fence_after();
-                }
-                if (lane == 0) {
-                    issue_pv<D>(tmem + 256 + 128 * qq, aP + qq * L::kP, aV16 + b * L::kV16, it > 0);
-                    mma_commit(&bars[kBOF + qq]);
-                    if (qq == nq - 1) mma_commit(&bars[kBVE + b]);
-                }
-                __syncwarp();
             }
+            if (ok && lane == 0) mma_commit(&bars[kBVE + b]);
+            __syncwarp();
         }
+    }
+
+    // back to the launch split (128 each) for the epilogue and the split merge
+    if (warp < 8) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 128;" ::: "memory");
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 128;" ::: "memory");
     }
 
     // ---------------------------------------------------------------- join
@@ -511,67 +552,62 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
             for (int st = 0; st < NST; ++st)
                 if (issued[st] > 0) mbar_wait(&bars[kBKVF + st], (uint32_t)((issued[st] - 1) & 1), p.timeout_ns);
         }
-    } else {
+    } else if (warp < 8 && q < nq) {
         // ------------------------------------------------------------ epilogue
-        if (warp < 8 && q < nq) {
-            const uint32_t tO = tmem + 256 + 128 * q;
-            const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-            const bool store = qrow < p.T;
-            const bool direct = p.splits == 1;
-            const float f = direct ? sv_ref / l_run : sv_ref;
-            const size_t prow_i = ((size_t)split * p.H + h) * p.Tstride + qrow;
-            float* dst = direct ? p.out + ((size_t)qrow * p.H + h) * D : p.part_o + prow_i * D;
+        const uint32_t tO = tmem + 256 + 128 * q + ((uint32_t)(wq * 32) << 16);
+        const bool store = qrow < p.T;
+        const bool direct = p.splits == 1;
+        const float f = direct ? sv_ref / l_run : sv_ref;
+        const size_t prow_i = ((size_t)split * p.H + h) * p.Tstride + qrow;
+        float* dst = direct ? p.out + ((size_t)qrow * p.H + h) * D : p.part_o + prow_i * D;
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t r[32];
-                tmem_ld32(tO + lane_off + cc * 32, r);
-                if (store) {
+        for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t r[32];
+            tmem_ld32(tO + cc * 32, r);
+            if (store) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4*>(dst + cc * 32 + e) =
-                            make_float4(__uint_as_float(r[e]) * f, __uint_as_float(r[e + 1]) * f,
-                                        __uint_as_float(r[e + 2]) * f, __uint_as_float(r[e + 3]) * f);
-                }
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4*>(dst + cc * 32 + e) =
+                        make_float4(__uint_as_float(r[e]) * f, __uint_as_float(r[e + 1]) * f,
+                                    __uint_as_float(r[e + 2]) * f, __uint_as_float(r[e + 3]) * f);
             }
-            if (store && !direct) *reinterpret_cast<float2*>(p.part_ml + prow_i * 2) = make_float2(m_run * a, l_run);
         }
+        if (store && !direct) *reinterpret_cast<float2*>(p.part_ml + prow_i * 2) = make_float2(m_run * a, l_run);
     }
-    {
+    if (p.splits > 1) {
         // Split merge.  Every CTA counts itself in, aborted or not, so the
-        // per-(head, pair) counter is back at zero after every call.
-        if (p.splits > 1) {
-            // the last split of this (head, query pair) to finish merges all partials
+        // per-(head, pair) counter is back at zero after every call; the last
+        // split of the (head, query pair) to arrive merges all partials.
+        __threadfence();
+        __syncthreads();
+        int* counter = p.counters + (size_t)h * (p.Tstride / 256) + pair;
+        if (tid == 0) *sLast = atomicAdd(counter, 1) == p.splits - 1;
+        __syncthreads();
+        if (*sLast) {
             __threadfence();
-            __syncthreads();
-            int* counter = p.counters + (size_t)h * (p.Tstride / 256) + pair;
-            if (tid == 0) *sLast = atomicAdd(counter, 1) == p.splits - 1;
-            __syncthreads();
-            if (*sLast) {
-                __threadfence();
-                const int rows = nq * 128;
-                for (int item = tid; item < rows * (D / 4); item += kAttendThreads) {
-                    const int rr = item / (D / 4), c4 = item % (D / 4);
-                    const int t = pair * 256 + rr;
-                    if (t >= p.T) continue;
-                    float M = -INFINITY;
-                    for (int s = 0; s < p.splits; ++s)
-                        M = fmaxf(M, __ldcg(p.part_ml + (((size_t)s * p.H + h) * p.Tstride + t) * 2));
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    float lsum = 0.f;
-                    for (int s = 0; s < p.splits; ++s) {
-                        const size_t pr = ((size_t)s * p.H + h) * p.Tstride + t;
-                        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + pr * 2));
-                        const float w = ex2_approx(ml.x - M);
-                        lsum += w * ml.y;
-                        const float4 o = __ldcg(reinterpret_cast<const float4*>(p.part_o + pr * D + c4 * 4));
-                        acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
-                    }
-                    const float inv = 1.f / lsum;
-                    *reinterpret_cast<float4*>(p.out + ((size_t)t * p.H + h) * D + c4 * 4) =
-                        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            const int rows = nq * 128;
+            for (int item = tid; item < rows * (D / 4); item += kAttendThreads) {
+                const int rr = item / (D / 4), c4 = item % (D / 4);
+                const int t = pair * 256 + rr;
+                if (t >= p.T) continue;
+                float M = -INFINITY;
+                for (int s = 0; s < p.splits; ++s)
+                    M = fmaxf(M, __ldcg(p.part_ml + (((size_t)s * p.H + h) * p.Tstride + t) * 2));
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                float lsum = 0.f;
+                for (int s = 0; s < p.splits; ++s) {
+                    const size_t pr = ((size_t)s * p.H + h) * p.Tstride + t;
+                    const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + pr * 2));
+                    const float w = ex2_approx(ml.x - M);
+                    lsum += w * ml.y;
+                    const float4 o = __ldcg(reinterpret_cast<const float4*>(p.part_o + pr * D + c4 * 4));
+                    acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
                 }
-                if (tid == 0) *counter = 0;
+                const float inv = 1.f / lsum;
+                *reinterpret_cast<float4*>(p.out + ((size_t)t * p.H + h) * D + c4 * 4) =
+                    make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
             }
+            if (tid == 0) *counter = 0;
         }
     }
     tc_fence_before();

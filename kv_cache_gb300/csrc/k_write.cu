@@ -8,7 +8,7 @@
 // "Runway Characters realtime on 4 H100", section "Кэш: 240 attention calls и
 // работа на запись").
 //
-// Launch: grid (CL, H, 2), one thread-block cluster of CL <= 8 CTAs per (head,
+// Launch: grid (CL, H, 2), one thread-block cluster of CL <= 16 CTAs per (head,
 // K|V).  The chunk's slots are cut into 16-slot groups aligned in the ring
 // (the V ring is slot-contiguous, so a group is one 16-byte store per head_dim
 // row); the groups are dealt to the cluster's CTAs in ring order.  Each CTA
@@ -209,10 +209,13 @@ __global__ void __launch_bounds__(kWriteThreads) write_kernel(const __grid_const
 }
 
 cudaError_t launch_write(const WriteParams& p, cudaStream_t s) {
-    const int CL = p.groups < 8 ? p.groups : 8;
+    // 16 CTAs per cluster (non-portable size, supported on this part) keep each
+    // CTA's share small: ~4 groups (64 rows) for a 757-token chunk.
+    const int CL = p.groups < 16 ? p.groups : 16;
     const int per = (p.groups + CL - 1) / CL;
-    const size_t smem = (size_t)per * 16 * p.d * (sizeof(uint16_t) + 2 * sizeof(float));   // rows + table rows
+    const size_t smem = (size_t)per * 16 * (size_t)p.d * 6;   // bf16 rows (2d bytes) + RoPE table rows (4d bytes)
     cudaError_t e = cudaFuncSetAttribute(write_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(write_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(CL, p.H, 2);
