@@ -83,12 +83,14 @@ cudaError_t launch_qprep(const QPrepParams& p, cudaStream_t s) {
 
 
 // ============================================================== K4: attention
-// One CTA of 14 warps per (head, pair of 128-row query tiles, KV split):
+// One CTA of 16 warps per (head, pair of 128-row query tiles, KV split):
 //   warps 0-3   softmax for query tile 0 (tensor-memory lanes 0-127 of S0, O0)
 //   warps 4-7   softmax for query tile 1 (S1, O1)
 //   warps 8-11  per tile: per-slot scales into shared memory, then V e4m3 -> fp16
 //   warp 12     TMA producer (the query tiles once, then K/V tiles, 3 stages)
 //   warp 13     tcgen05 issuer
+//   warps 14-15 idle (they keep two softmax warps and two others on every SM
+//               sub-partition, which the register split needs)
 // Tensor memory (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [384,384+d).
 // The softmax reads its S row once, writes P as packed fp16 back over the first
 // 64 columns of S, and O_q += P_q V runs with A in tensor memory.  The issuer
@@ -143,7 +145,7 @@ enum : int {
 };
 enum : int { kWaitQ = 1, kWaitKVFull = 2, kWaitKVEmpty = 3, kWaitS = 4, kWaitP = 5, kWaitO = 6, kWaitV16Full = 7,
              kWaitV16Empty = 8, kWaitCol = 9 };
-constexpr int kAttendThreads = 448;
+constexpr int kAttendThreads = 512;
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -276,13 +278,14 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
     for (int st = 0; st < NST; ++st) issued[st] = 0;
     bool q_issued = false;
 
-    // Register split: the launch gives every thread 128 registers (448 x 128 =
-    // 57,344); the 6 non-softmax warps drop to 64 and the 8 softmax warps take
-    // 168 (192 x 64 + 256 x 168 = 55,296), so the increase always fits.
+    // Register split.  The launch gives each of the 16 warps 128 registers per
+    // thread, and every SM sub-partition (warps w, w+4, w+8, w+12) holds two
+    // softmax warps and two others; 2 x 184 + 2 x 72 = 2 x 128 + 2 x 128, so the
+    // increase always fits in the registers its own sub-partition released.
     if (warp < 8) {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 168;" ::: "memory");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 184;" ::: "memory");
     } else {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 64;" ::: "memory");
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
     }
 
     if (warp < 8) {
@@ -481,7 +484,7 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
             }
             __syncwarp();
         }
-    } else {
+    } else if (warp == 13) {
         // ------------------------------------------------------------ MMA issuer
         const uint32_t aQ = smem_u32(sQ);
         const uint32_t aK = smem_u32(sK);
