@@ -532,17 +532,19 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
         }
     }
 
-    // back to the launch split (128 each) for the epilogue and the split merge
+    // ---------------------------------------------------------------- join
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // Back to the launch split (128 each) for the epilogue and the split merge.
+    // Only after the barrier: a warp that asked for its registers back earlier
+    // could take them before a softmax warp of its sub-partition had made its
+    // own increase, and that increase would then never be granted.
     if (warp < 8) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 128;" ::: "memory");
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 128;" ::: "memory");
     }
-
-    // ---------------------------------------------------------------- join
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
     const bool aborted = *sAbort != 0;
     if (aborted) {
         // nothing of ours may still be in flight when the CTA exits
