@@ -14,7 +14,7 @@
 //  * S = Q K^T runs on tcgen05 (kind::f8f6f4, M = N = 128) into tensor memory.
 //  * Thread i owns query row i (tensor-memory lane i): it reads S, applies the
 //    per-slot K scale, keeps a running max m and sum l (online softmax; the max
-//    is only moved when it grows by more than 2^8, so O is rarely rescaled),
+//    is only moved when it grows by more than 2^15, so O is rarely rescaled),
 //    and writes P = 2^(x - m) * (V scale of the slot / V scale reference) as
 //    fp16 into shared memory.
 //  * The V tile is widened from e4m3 to fp16 in shared memory (exact), and
@@ -86,7 +86,7 @@ cudaError_t launch_qprep(const QPrepParams& p, cudaStream_t s) {
 // One CTA of 16 warps per (head, pair of 128-row query tiles, KV split):
 //   warps 0-3   softmax for query tile 0 (tensor-memory lanes 0-127 of S0, O0)
 //   warps 4-7   softmax for query tile 1 (S1, O1)
-//   warps 8-11  per tile: per-slot scales into shared memory, then V e4m3 -> fp16
+//   warps 8-11  V e4m3 -> fp16 per tile (bit operations, giving V * 2^-8 exactly)
 //   warp 12     TMA producer (the query tiles once, then K/V tiles, 3 stages)
 //   warp 13     tcgen05 issuer
 //   warps 14-15 idle (they keep two softmax warps and two others on every SM
@@ -106,28 +106,15 @@ struct AttendSmem {
     static constexpr int kK = 128 * D;            // K tile [128 slots][D], e4m3
     static constexpr int kV = D * 128;            // V tile [D][128 slots], e4m3
     static constexpr int kV16 = D * 128 * 2;      // V tile in fp16: 2 K-blocks of [D][64]
-    static constexpr int kCol = 2 * 128 * 4 + 4 * 4 * 4;   // per-slot k scale, V ratio; 4 group records
     static constexpr int offQ = 0;
     static constexpr int offK = offQ + 2 * kQ;
     static constexpr int offV = offK + kStages * kK;
     static constexpr int offV16 = offV + kStages * kV;
-    static constexpr int offCol = offV16 + 2 * kV16;
-    static constexpr int offBar = offCol + 2 * kCol;
-    static constexpr int kBars = 20;
+    static constexpr int offBar = offV16 + 2 * kV16;
+    static constexpr int kBars = 18;
     static constexpr int offMisc = offBar + kBars * 8;
     static constexpr int kBytes = offMisc + 64;
     static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
-};
-
-// Per-tile scale record written by the converter warps: for column c, the K scale
-// ks[c] and the V ratio rr[c] = (V scale) / (reference); for each 32-column group
-// g, whether all its columns are valid and share one (ks, rr), and then that
-// pair with 1/rr and log2(rr).
-struct ColInfo {
-    float ks[128];
-    float rr[128];
-    float gks[4], glg[4], gri[4];
-    int guni[4];
 };
 
 // mbarrier slots
@@ -135,16 +122,15 @@ enum : int {
     kBQ = 0,        // query tiles landed (TMA)
     kBKVF = 1,      // [3] K/V stage full (TMA)
     kBKVE = 4,      // [3] K/V stage free: S MMAs done (commit) + 128 converter arrivals
-    kBSF = 7,       // [2] S_q computed (commit)
+    kBSF = 7,       // [2] S_q computed, and the O_q += P_q V before it (commit)
     kBPF = 9,       // [2] P_q in tensor memory (128 softmax arrivals)
-    kBOF = 11,      // [2] O_q += P_q V done (commit)
+    kBOF = 11,      // [2] last O_q += P_q V done (commit)
     kBVF = 13,      // [2] fp16 V buffer full (128 converter arrivals)
-    kBVE = 15,      // [2] fp16 V buffer and scale record free (commit after both PV MMAs)
-    kBCF = 17,      // [2] scale record of the tile written (128 converter arrivals)
-    kBDrain = 19,   // drain after an abort
+    kBVE = 15,      // [2] fp16 V buffer free (commit after both PV MMAs)
+    kBDrain = 17,   // drain after an abort
 };
 enum : int { kWaitQ = 1, kWaitKVFull = 2, kWaitKVEmpty = 3, kWaitS = 4, kWaitP = 5, kWaitO = 6, kWaitV16Full = 7,
-             kWaitV16Empty = 8, kWaitCol = 9 };
+             kWaitV16Empty = 8 };
 constexpr int kAttendThreads = 512;
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -158,7 +144,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
                                           const AttendParams& p, int site) {
     int ok = 1;
     if ((threadIdx.x & 31) == 0) {
-        if (!mbar_try_wait(bar, parity)) {
+        if (!mbar_test_wait(bar, parity) && !mbar_try_wait(bar, parity)) {
             const uint64_t t0 = globaltimer_ns();
             while (true) {
                 if (mbar_try_wait(bar, parity)) break;
@@ -205,6 +191,12 @@ __device__ __forceinline__ float lg2_approx(float x) {
     return y;
 }
 
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
 template <int D>
@@ -218,7 +210,6 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
     uint8_t* sK = smem + L::offK;
     uint8_t* sV = smem + L::offV;
     uint8_t* sV16 = smem + L::offV16;
-    ColInfo* sCol = reinterpret_cast<ColInfo*>(smem + L::offCol);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::offBar);
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + L::offMisc);
     volatile int* sAbort = reinterpret_cast<volatile int*>(smem + L::offMisc + 4);
@@ -243,7 +234,7 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
 
     if (warp == 0) tmem_alloc(sTmem, 512);
     if (tid == 0) {
-        const int counts[L::kBars] = {1, 1, 1, 1, 129, 129, 129, 1, 1, 128, 128, 1, 1, 128, 128, 1, 1, 128, 128, 1};
+        const int counts[L::kBars] = {1, 1, 1, 1, 129, 129, 129, 1, 1, 128, 128, 1, 1, 128, 128, 1, 1, 1};
         for (int b = 0; b < L::kBars; ++b) mbar_init(&bars[b], counts[b]);
         fence_mbar_init();
         *sAbort = 0;
@@ -295,102 +286,157 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
         const uint32_t tS = tmem + 128 * q + lane_off;
         const uint32_t tO = tmem + 256 + 128 * q + lane_off;
         a = scale_of(__ldg(p.qamax + (size_t)h * p.Tstride + qrow)) * p.log2e_rsqrt_d;
+        // Per-slot scales of a tile, held by the warp: lane e has columns e, 32+e,
+        // 64+e, 96+e (one per 32-column group).  The next tile's amax values are
+        // loaded while the current tile is processed.
+        float kan[4], van[4];
+        auto load_amax = [&](int it2) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const int s = (j0 + it2) * 128 + g * 32 + lane;
+                const bool v = it2 < nt && s < p.count;
+                kan[g] = v ? __ldg(kam + s) : -1.f;
+                van[g] = v ? __ldg(vam + s) : -1.f;
+            }
+        };
+        if (active) load_amax(0);
         for (int it = 0; active && it < nt; ++it) {
-            const int b = it & 1;
             const int nvalid = min(128, p.count - (j0 + it) * 128);
-            if (!warp_wait(&bars[kBCF + b], (uint32_t)((it >> 1) & 1), sAbort, p, kWaitCol)) break;
-            const ColInfo& ci = sCol[b];
+            // this tile's scales: k scale, V ratio and its reciprocal per column, and
+            // per group whether all 32 columns are valid and share one pair
+            // (amax * (1/448) is within one fp32 rounding of amax / 448, which is all
+            // the attention needs; amax == 0 means scale 1)
+            float ksv[4], rrv[4], riv[4], gks[4], glg[4], gri[4];
+            bool uni[4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const bool valid = kan[g] >= 0.f;
+                constexpr float k1_448 = 1.f / 448.f;
+                ksv[g] = valid ? (kan[g] == 0.f ? 1.f : kan[g] * k1_448) : 0.f;
+                rrv[g] = valid ? (van[g] == 0.f ? 1.f : van[g] * k1_448) * inv_sv_ref : 0.f;
+                riv[g] = valid ? rcp_approx(rrv[g]) : 0.f;
+                gks[g] = __shfl_sync(0xffffffffu, ksv[g], 0);
+                const float r0 = __shfl_sync(0xffffffffu, rrv[g], 0);
+                uni[g] = __all_sync(0xffffffffu, valid && ksv[g] == gks[g] && rrv[g] == r0);
+                glg[g] = uni[g] ? lg2_approx(r0) : 0.f;
+                gri[g] = __shfl_sync(0xffffffffu, riv[g], 0);
+            }
+            load_amax(it + 1);
             if (!warp_wait(&bars[kBSF + q], (uint32_t)(it & 1), sAbort, p, kWaitS)) break;
             tc_fence_after();
+            // pass 1: row max of raw * k_scale (two groups per tensor-memory wait);
+            // per uniform group also its largest raw value
+            float tm = -INFINITY;
+            float graw[4];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t ra[32], rb[32];
+                tmem_ld32_async(tS + hh * 64, ra);
+                tmem_ld32_async(tS + hh * 64 + 32, rb);
+                tmem_wait_ld_dep(ra);
+                tmem_dep(rb);
+#pragma unroll
+                for (int k2 = 0; k2 < 2; ++k2) {
+                    const int g = hh * 2 + k2;
+                    const uint32_t* r = k2 == 0 ? ra : rb;
+                    if (uni[g]) {
+                        float m0 = fmax3(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]));
+                        float m1 = fmax3(__uint_as_float(r[3]), __uint_as_float(r[4]), __uint_as_float(r[5]));
+                        float m2 = fmax3(__uint_as_float(r[6]), __uint_as_float(r[7]), __uint_as_float(r[8]));
+                        float m3 = fmax3(__uint_as_float(r[9]), __uint_as_float(r[10]), __uint_as_float(r[11]));
+#pragma unroll
+                        for (int e = 12; e < 28; e += 8) {
+                            m0 = fmax3(m0, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+                            m1 = fmax3(m1, __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+                            m2 = fmax3(m2, __uint_as_float(r[e + 4]), __uint_as_float(r[e + 5]));
+                            m3 = fmax3(m3, __uint_as_float(r[e + 6]), __uint_as_float(r[e + 7]));
+                        }
+                        m0 = fmax3(m0, __uint_as_float(r[28]), __uint_as_float(r[29]));
+                        m1 = fmax3(m1, __uint_as_float(r[30]), __uint_as_float(r[31]));
+                        graw[g] = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+                        tm = fmaxf(tm, graw[g] * gks[g]);
+                    } else {
+                        graw[g] = 0.f;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const float ks = __shfl_sync(0xffffffffu, ksv[g], e);
+                            if (g * 32 + e < nvalid) tm = fmaxf(tm, __uint_as_float(r[e]) * ks);
+                        }
+                    }
+                }
+            }
+            // Lazy running max: moved only when the row max grows by more than 2^15
+            // (so P stays below 2^15 < 65504, finite in fp16); then O and the row sum
+            // are rescaled.  Tensor-memory access is warp-collective.  O_q is stable
+            // here: S_q(j) was issued behind O_q += P_q(j-1) V and has completed.
+            const bool first = m_run == -INFINITY;
+            const bool grow = !first && (tm - m_run) * a > 15.f;
+            if (__any_sync(0xffffffffu, grow)) {
+                const float alpha = grow ? ex2_approx((m_run - tm) * a) : 1.f;
+                if (it > 0) {
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + cc * 32, o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(tO + cc * 32, o);
+                    }
+                }
+                l_run *= alpha;
+            }
+            if (first || grow) m_run = tm;
+            const float ma = m_run * a;
+            // pass 2: P = 2^(x - m) * (V scale ratio) as fp16, over S in tensor memory.
+            // The row sum must use the same (rounded) weights that O += P V sees
+            // wherever one weight dominates: it sums the fp32 P and adds back the fp16
+            // rounding of each group's largest element (the row's dominant weight is
+            // always one of them); the other elements' rounding is at most 2^-12 of
+            // their own, non-dominant, share.
             float lsum = 0.f;
             uint32_t r[32], rn[32];
             tmem_ld32(tS, r);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
                 if (g < 3) tmem_ld32_async(tS + (g + 1) * 32, rn);
-                const bool uni = ci.guni[g] != 0;
-                // group max of raw * k_scale
-                float gm;
-                if (uni) {
-                    float m0 = fmax3(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]));
-                    float m1 = fmax3(__uint_as_float(r[3]), __uint_as_float(r[4]), __uint_as_float(r[5]));
-#pragma unroll
-                    for (int e = 6; e < 30; e += 4) {
-                        m0 = fmax3(m0, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
-                        m1 = fmax3(m1, __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
-                    }
-                    gm = fmax3(m0, m1, fmaxf(__uint_as_float(r[30]), __uint_as_float(r[31]))) * ci.gks[g];
-                } else {
-                    gm = -INFINITY;
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (g * 32 + e < nvalid) gm = fmaxf(gm, __uint_as_float(r[e]) * ci.ks[g * 32 + e]);
-                }
-                // lazy running max: moved only when it grows by more than 2^8; then O,
-                // the sums and this tile's P so far are rescaled (all warp-collective)
-                const bool first = m_run == -INFINITY;
-                const bool grow = !first && gm != -INFINITY && (gm - m_run) * a > 8.f;
-                if (__any_sync(0xffffffffu, grow)) {
-                    const float alpha = grow ? ex2_approx((m_run - gm) * a) : 1.f;
-                    tmem_wait_st();
-                    if (it > 0) {
-#pragma unroll
-                        for (int cc = 0; cc < D / 32; ++cc) {
-                            uint32_t o[32];
-                            tmem_ld32(tO + cc * 32, o);
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                            tmem_st32(tO + cc * 32, o);
-                        }
-                    }
-                    const __half2 a2 = __float2half2_rn(alpha);
-                    for (int pg = 0; pg < g; ++pg) {
-                        uint32_t pp[16];
-                        tmem_ld16(tS + pg * 16, pp);
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            uint32_t w = pp[e];
-                            __half2 hv = *reinterpret_cast<__half2*>(&w);
-                            hv = __hmul2(hv, a2);
-                            pp[e] = h2_bits(hv);
-                        }
-                        tmem_st16(tS + pg * 16, pp);
-                    }
-                    tmem_wait_st();
-                    l_run *= alpha;
-                    lsum *= alpha;
-                }
-                if (first || grow) m_run = gm;
-                const float ma = m_run * a;
-                // P = 2^(x - m) * (V scale ratio) as fp16; the row sum adds the rounded P
-                // over the ratio, the same weights that O += P V sees.
                 uint32_t pk[16];
-                if (uni) {
-                    const float c1 = ci.gks[g] * a;
-                    const float c0 = ci.glg[g] - ma;
+                if (uni[g]) {
+                    const float c1 = gks[g] * a;
+                    const float c0 = glg[g] - ma;
                     const float2 c1v = make_float2(c1, c1), c0v = make_float2(c0, c0);
-                    float2 acc = make_float2(0.f, 0.f);
+                    float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const float2 x = ffma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c1v, c0v);
-                        const __half2 hv = __floats2half2_rn(ex2_approx(x.x), ex2_approx(x.y));
-                        pk[e / 2] = h2_bits(hv);
-                        acc = fadd2(acc, __half22float2(hv));
+                    for (int e = 0; e < 32; e += 4) {
+                        const float2 x01 = ffma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c1v, c0v);
+                        const float2 x23 = ffma2(make_float2(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])), c1v, c0v);
+                        const float2 p01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
+                        const float2 p23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
+                        pk[e / 2] = h2_bits(__floats2half2_rn(p01.x, p01.y));
+                        pk[e / 2 + 1] = h2_bits(__floats2half2_rn(p23.x, p23.y));
+                        s0 = fadd2(s0, p01);
+                        s1 = fadd2(s1, p23);
                     }
-                    lsum += (acc.x + acc.y) * ci.gri[g];
+                    const float pm = ex2_approx(fmaf(graw[g], c1, c0));
+                    const float corr = __half2float(__float2half_rn(pm)) - pm;
+                    lsum += ((s0.x + s0.y) + (s1.x + s1.y) + corr) * gri[g];
                 } else {
+                    // columns of two chunks, or past the valid slots: per-column scales
+                    // (V ratio 0 beyond the valid slots, so those P are exactly 0; the
+                    // exponent is capped at 64 so that 2^x stays finite there)
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const int c = g * 32 + e;
-                        const bool v0 = c < nvalid, v1 = c + 1 < nvalid;
-                        const float r0 = ci.rr[c], r1 = ci.rr[c + 1];
-                        const float p0 = v0 ? ex2_approx(fmaf(__uint_as_float(r[e]) * ci.ks[c], a, -ma)) * r0 : 0.f;
-                        const float p1 = v1 ? ex2_approx(fmaf(__uint_as_float(r[e + 1]) * ci.ks[c + 1], a, -ma)) * r1 : 0.f;
+                        const float ks0 = __shfl_sync(0xffffffffu, ksv[g], e);
+                        const float ks1 = __shfl_sync(0xffffffffu, ksv[g], e + 1);
+                        const float r0 = __shfl_sync(0xffffffffu, rrv[g], e);
+                        const float r1 = __shfl_sync(0xffffffffu, rrv[g], e + 1);
+                        const float i0 = __shfl_sync(0xffffffffu, riv[g], e);
+                        const float i1 = __shfl_sync(0xffffffffu, riv[g], e + 1);
+                        const float p0 = ex2_approx(fminf(fmaf(__uint_as_float(r[e]) * ks0, a, -ma), 64.f)) * r0;
+                        const float p1 = ex2_approx(fminf(fmaf(__uint_as_float(r[e + 1]) * ks1, a, -ma), 64.f)) * r1;
                         const __half2 hv = __floats2half2_rn(p0, p1);
                         pk[e / 2] = h2_bits(hv);
                         const float2 back = __half22float2(hv);
-                        if (v0) lsum += __fdiv_rn(back.x, r0);
-                        if (v1) lsum += __fdiv_rn(back.y, r1);
+                        lsum = fmaf(back.x, i0, fmaf(back.y, i1, lsum));
                     }
                 }
                 tmem_st16(tS + g * 16, pk);     // P group g -> columns [16g, 16g + 16) of S_q
@@ -406,35 +452,17 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
             mbar_arrive(&bars[kBPF + q]);
         }
         if (active && !*sAbort) {
-            if (warp_wait(&bars[kBOF + q], (uint32_t)((nt - 1) & 1), sAbort, p, kWaitO)) tc_fence_after();
+            // O_q is complete once the last O_q += P_q V has finished (its commit is
+            // the only arrival on this barrier)
+            if (warp_wait(&bars[kBOF + q], 0u, sAbort, p, kWaitO)) tc_fence_after();
         }
     } else if (warp < 12) {
-        // ------------------------------------------------------------ scales, then V e4m3 -> fp16
+        // ------------------------------------------------------------ V e4m3 -> fp16
         const int c0 = tid - 256;
-        const int cw = warp - 8;
         for (int it = 0; it < nt; ++it) {
             const int st = it % NST, b = it & 1;
             if (it >= 2 && !warp_wait(&bars[kBVE + b], (uint32_t)(((it >> 1) - 1) & 1), sAbort, p, kWaitV16Empty))
                 break;
-            {
-                const int s = (j0 + it) * 128 + c0;
-                const bool valid = s < p.count;
-                const float ks = valid ? scale_of(__ldg(kam + s)) : 0.f;
-                const float rr = valid ? __fmul_rn(scale_of(__ldg(vam + s)), inv_sv_ref) : 0.f;
-                ColInfo& ci = sCol[b];
-                ci.ks[c0] = ks;
-                ci.rr[c0] = rr;
-                const float KS = __shfl_sync(0xffffffffu, ks, 0);
-                const float RR = __shfl_sync(0xffffffffu, rr, 0);
-                const bool uni = __all_sync(0xffffffffu, valid && ks == KS && rr == RR);
-                if (lane == 0) {
-                    ci.gks[cw] = KS;
-                    ci.glg[cw] = uni ? lg2_approx(RR) : 0.f;
-                    ci.gri[cw] = uni ? __frcp_rn(RR) : 0.f;
-                    ci.guni[cw] = uni ? 1 : 0;
-                }
-                mbar_arrive(&bars[kBCF + b]);
-            }
             if (!warp_wait(&bars[kBKVF + st], (uint32_t)((it / NST) & 1), sAbort, p, kWaitKVFull)) break;
             const uint8_t* src = sV + st * L::kV;
             uint8_t* dst = sV16 + b * L::kV16;
@@ -443,13 +471,16 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                 const int dd = qq >> 3, c = qq & 7;
                 const uint4 w = *reinterpret_cast<const uint4*>(src + dd * 128 + ((c ^ (dd & 7)) << 4));
                 const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                // e4m3 -> fp16 with integer operations: sign to bit 15, the other 7 bits
+                // to bits 7-13, which is the fp16 code of value * 2^-8 (subnormals
+                // included); the 2^8 is applied to O at the end
                 uint32_t h16[8];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(ws[e] & 0xFFFFu), __NV_E4M3);
-                    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(ws[e] >> 16), __NV_E4M3);
-                    h16[2 * e] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
-                    h16[2 * e + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
+                    const uint32_t lo = __byte_perm(ws[e], 0u, 0x1404u);   // [0, b0, 0, b1]
+                    const uint32_t hi = __byte_perm(ws[e], 0u, 0x3424u);   // [0, b2, 0, b3]
+                    h16[2 * e] = (lo & 0x80008000u) | ((lo >> 1) & 0x3F803F80u);
+                    h16[2 * e + 1] = (hi & 0x80008000u) | ((hi >> 1) & 0x3F803F80u);
                 }
                 uint8_t* dblk = dst + (c >> 2) * (D * 128) + dd * 128;
                 const int cb = (c & 3) * 2;
@@ -501,8 +532,17 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
             }
             __syncwarp();
         }
+        // Per tile j and query tile q: O_q += P_q(j) V_j goes out as soon as P_q(j)
+        // is in tensor memory, followed directly by S_q(j+1) = Q_q K_{j+1}^T, and
+        // one commit covers both (a commit holds the issuing thread until the
+        // tensor pipe has taken the MMAs in, so there are as few as possible).
         for (int it = 0; ok && it < nt; ++it) {
             const int stn = (it + 1) % NST, b = it & 1;
+            const bool has_next = it + 1 < nt;
+            if (has_next) {
+                ok = warp_wait(&bars[kBKVF + stn], (uint32_t)(((it + 1) / NST) & 1), sAbort, p, kWaitKVFull);
+                if (!ok) break;
+            }
             ok = warp_wait(&bars[kBVF + b], (uint32_t)((it >> 1) & 1), sAbort, p, kWaitV16Full);
             for (int qq = 0; qq < nq && ok; ++qq) {
                 ok = warp_wait(&bars[kBPF + qq], (uint32_t)(it & 1), sAbort, p, kWaitP);
@@ -510,25 +550,19 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                 tc_fence_after();
                 if (lane == 0) {
                     issue_pv<D>(tmem + 256 + 128 * qq, tmem + 128 * qq, aV16 + b * L::kV16, it > 0);
-                    mma_commit(&bars[kBOF + qq]);
-                }
-                __syncwarp();
-                if (it + 1 < nt) {
-                    if (qq == 0) {
-                        ok = warp_wait(&bars[kBKVF + stn], (uint32_t)(((it + 1) / NST) & 1), sAbort, p, kWaitKVFull);
-                        if (!ok) break;
-                        tc_fence_after();
-                    }
-                    if (lane == 0) {
+                    if (has_next) {
                         issue_s<D>(tmem + 128 * qq, aQ + qq * L::kQ, aK + stn * L::kK);
                         mma_commit(&bars[kBSF + qq]);
-                        if (qq == nq - 1) mma_commit(&bars[kBKVE + stn]);
+                    } else {
+                        mma_commit(&bars[kBOF + qq]);
                     }
-                    __syncwarp();
+                    if (qq == nq - 1) {
+                        if (has_next) mma_commit(&bars[kBKVE + stn]);
+                        mma_commit(&bars[kBVE + b]);
+                    }
                 }
+                __syncwarp();
             }
-            if (ok && lane == 0) mma_commit(&bars[kBVE + b]);
-            __syncwarp();
         }
     }
 
@@ -562,7 +596,7 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
         const uint32_t tO = tmem + 256 + 128 * q + ((uint32_t)(wq * 32) << 16);
         const bool store = qrow < p.T;
         const bool direct = p.splits == 1;
-        const float f = direct ? sv_ref / l_run : sv_ref;
+        const float f = direct ? 256.f * sv_ref / l_run : 256.f * sv_ref;   // V was widened as V * 2^-8
         const size_t prow_i = ((size_t)split * p.H + h) * p.Tstride + qrow;
         float* dst = direct ? p.out + ((size_t)qrow * p.H + h) * D : p.part_o + prow_i * D;
 #pragma unroll
