@@ -158,6 +158,44 @@ int kvring_launch_count(const kvring_t* ring, uint64_t* out);
  * copies in flight, frees its tensor memory and returns.  Errors: EINVAL. */
 int kvring_debug_fault(kvring_t* ring, int32_t skip_tile, int64_t timeout_ns);
 
+/* Attention over a caller-held cache that allocates nothing.
+ *
+ * The pages have no counterpart to this call; it exists for callers that may
+ * not allocate device memory (no cudaMalloc/cudaFree, no allocating library
+ * routine) because their own arena or pool owns all of it, e.g. a serving
+ * engine that places the FP8 cache in a slab it carved out itself.  It runs the
+ * same Q preparation and FP8 attention as kvring_attend on one layer's cache,
+ * given in these layouts (all device memory, caller-owned):
+ *   k8:    e4m3 codes [H][slots_padded][d], slot-major rows, K already rotated
+ *   vt8:   e4m3 codes [H][d][slots_padded], slot-contiguous rows
+ *   kamax, vamax: fp32 [H][slots_padded], the chunk amax of each slot
+ *          (scale = amax / 448, amax 0 meaning scale 1)
+ *   rope:  fp32 (cos, sin) pairs [rows][d/2] with rows > q_pos0 + n_q - 1;
+ *          entry [p][i] = fp32(cos(p * w_i)), fp32(sin(p * w_i)), angle and
+ *          cosine in float64, w_i = theta^(-2i/d) (the table kvring_create builds)
+ *   q_bf16: [n_q][H][d]; query i sits at position q_pos0 + i
+ *   out_f32: [n_q][H][d]
+ * Slots [0, count) are attended; slots_padded is a multiple of 128 and the pad
+ * slots' V codes must be finite (zero).  k8, vt8, q and out are 16-byte aligned.
+ * err_word: 4 ints, set to KVRING_ETIMEOUT (and kernel, wait site, block) if a
+ * bounded device wait runs out; NULL leaves such time-outs unreported.
+ *
+ * Its only scratch is a fixed array inside the library (the e4m3 Q rows and
+ * their amax): 16,384 rows of (head, query padded to 256), i.e. 2.06 MB that
+ * every GPU loading the library holds until the process exits.  Larger calls
+ * are rejected with KVRING_EINVAL.  The first call on a device looks up that
+ * array's device address (once per device); make that first call before any
+ * stream capture.  Every call shares the array and leaves its last contents
+ * there; each call rewrites all of it that it reads, but calls that overlap on
+ * the GPU (other streams, other threads) race and must be serialised by the
+ * caller.  Uses a single KV split, so for few heads it fills fewer SMs than
+ * kvring_attend.  Asynchronous on cuda_stream.  Errors (message in
+ * kvring_last_error(NULL)): EINVAL, ENODEV, ECUDA. */
+int kvring_attend_noalloc(const void* k8, const void* vt8, const float* kamax, const float* vamax,
+                          const float* rope, int64_t q_pos0, const void* q_bf16, int32_t n_q,
+                          int32_t num_heads, int32_t head_dim, int32_t slots_padded, int32_t count,
+                          float* out_f32, int* err_word, void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -154,6 +154,17 @@ int choose_splits(const kvring_t* r, int units, int ntiles) {
 
 }  // namespace
 
+namespace kvring_impl {
+// Message reported by kvring_last_error(NULL) for calls that have no ring.
+void set_thread_error(const std::string& msg) { g_create_error = msg; }
+
+// 3-D tiled tensor map over uint8 data (the rings and Q tiles); KVRING_OK or KVRING_ECUDA.
+int encode_u8_map(CUtensorMap* map, void* base, const cuuint64_t dims[3], const cuuint64_t strides[2],
+                  const cuuint32_t box[3], CUtensorMapSwizzle swz) {
+    return make_map(nullptr, map, base, dims, strides, box, swz);
+}
+}  // namespace kvring_impl
+
 extern "C" {
 
 int kvring_create(const kvring_config* cfg_in, kvring_t** out) {

@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <stdint.h>
 
+#include <string>
+
 #include "../../include/kvring.h"
 
 namespace kvring_impl {
@@ -87,5 +89,10 @@ struct AttendMaps {
 cudaError_t launch_attend(const AttendParams& p, const AttendMaps& maps, cudaStream_t s);
 
 size_t attend_smem_bytes(int d);
+
+// Shared by the host translation units.
+void set_thread_error(const std::string& msg);
+int encode_u8_map(CUtensorMap* map, void* base, const cuuint64_t dims[3], const cuuint64_t strides[2],
+                  const cuuint32_t box[3], CUtensorMapSwizzle swz);
 
 }  // namespace kvring_impl

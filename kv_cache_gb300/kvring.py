@@ -83,6 +83,8 @@ _SIGNATURES = {
     "kvring_last_error": (ctypes.c_char_p, [_P]),
     "kvring_debug_fault": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int64]),
     "kvring_launch_count": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint64)]),
+    "kvring_attend_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int64, _P, ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P, _P]),
 }
 
 
@@ -201,6 +203,31 @@ def kvring_launch_count(ring) -> int:
 
 def kvring_debug_fault(ring, skip_tile: int, timeout_ns: int) -> None:
     _check(load().kvring_debug_fault(ring, skip_tile, timeout_ns), ring)
+
+
+def kvring_attend_noalloc(k8, vt8, kamax, vamax, rope, q_pos0: int, q, out, count: int, err=None,
+                          stream=None) -> None:
+    """Attention over a caller-held one-layer cache without any device allocation.
+
+    k8 uint8 [H, slots_padded, d], vt8 uint8 [H, d, slots_padded], kamax/vamax
+    float32 [H, slots_padded], rope float32 [rows, d/2, 2], q bf16 [n_q, H, d],
+    out float32 [n_q, H, d], err int32 [4] or None -- all CUDA tensors the caller
+    owns (see include/kvring.h for the layouts and the fixed scratch limit).
+    """
+    n_q, H, d = (int(x) for x in q.shape)
+    slots_padded = int(k8.shape[1])
+    qp = _dev_bf16(q, n_q, H, d, "q")
+    for name, t, shape in (("k8", k8, (H, slots_padded, d)), ("vt8", vt8, (H, d, slots_padded)),
+                           ("kamax", kamax, (H, slots_padded)), ("vamax", vamax, (H, slots_padded)),
+                           ("out", out, (n_q, H, d))):
+        if not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor of shape {shape}")
+    if not rope.is_cuda or not rope.is_contiguous() or rope.shape[1:] != (d // 2, 2):
+        raise ValueError(f"rope must be a contiguous CUDA tensor of shape (rows, {d // 2}, 2)")
+    rc = load().kvring_attend_noalloc(k8.data_ptr(), vt8.data_ptr(), kamax.data_ptr(), vamax.data_ptr(),
+                                      rope.data_ptr(), int(q_pos0), qp, n_q, H, d, slots_padded, int(count),
+                                      out.data_ptr(), err.data_ptr() if err is not None else None, _stream(stream))
+    _check(rc, None)
 
 
 class KVRing:
