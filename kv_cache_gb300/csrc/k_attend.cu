@@ -132,6 +132,7 @@ enum : int {
 enum : int { kWaitQ = 1, kWaitKVFull = 2, kWaitKVEmpty = 3, kWaitS = 4, kWaitP = 5, kWaitO = 6, kWaitV16Full = 7,
              kWaitV16Empty = 8 };
 constexpr int kAttendThreads = 512;
+constexpr int kMaxSplits = 4;   // KV splits per (head, query pair); the merge keeps them all in registers
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -624,27 +625,50 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
         __syncthreads();
         if (*sLast) {
             __threadfence();
+            // each item is 16 output values of one row; all splits' partials for it
+            // are loaded before any is used (at most kMaxSplits of them)
             const int rows = nq * 128;
-            for (int item = tid; item < rows * (D / 4); item += kAttendThreads) {
-                const int rr = item / (D / 4), c4 = item % (D / 4);
+            for (int item = tid; item < rows * (D / 16); item += kAttendThreads) {
+                const int rr = item / (D / 16), c16 = item % (D / 16);
                 const int t = pair * 256 + rr;
                 if (t >= p.T) continue;
+                float2 ml[kMaxSplits];
+                float4 o[kMaxSplits][4];
+#pragma unroll
+                for (int sp = 0; sp < kMaxSplits; ++sp) {
+                    if (sp < p.splits) {
+                        const size_t pr = ((size_t)sp * p.H + h) * p.Tstride + t;
+                        ml[sp] = __ldcg(reinterpret_cast<const float2*>(p.part_ml + pr * 2));
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4)
+                            o[sp][k4] = __ldcg(reinterpret_cast<const float4*>(p.part_o + pr * D + c16 * 16 + k4 * 4));
+                    }
+                }
                 float M = -INFINITY;
-                for (int s = 0; s < p.splits; ++s)
-                    M = fmaxf(M, __ldcg(p.part_ml + (((size_t)s * p.H + h) * p.Tstride + t) * 2));
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int sp = 0; sp < kMaxSplits; ++sp)
+                    if (sp < p.splits) M = fmaxf(M, ml[sp].x);
                 float lsum = 0.f;
-                for (int s = 0; s < p.splits; ++s) {
-                    const size_t pr = ((size_t)s * p.H + h) * p.Tstride + t;
-                    const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + pr * 2));
-                    const float w = ex2_approx(ml.x - M);
-                    lsum += w * ml.y;
-                    const float4 o = __ldcg(reinterpret_cast<const float4*>(p.part_o + pr * D + c4 * 4));
-                    acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
+                float4 acc[4];
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) acc[k4] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int sp = 0; sp < kMaxSplits; ++sp) {
+                    if (sp < p.splits) {
+                        const float w = ex2_approx(ml[sp].x - M);
+                        lsum += w * ml[sp].y;
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4) {
+                            acc[k4].x += w * o[sp][k4].x; acc[k4].y += w * o[sp][k4].y;
+                            acc[k4].z += w * o[sp][k4].z; acc[k4].w += w * o[sp][k4].w;
+                        }
+                    }
                 }
                 const float inv = 1.f / lsum;
-                *reinterpret_cast<float4*>(p.out + ((size_t)t * p.H + h) * D + c4 * 4) =
-                    make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                float4* dst = reinterpret_cast<float4*>(p.out + ((size_t)t * p.H + h) * D + c16 * 16);
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4)
+                    dst[k4] = make_float4(acc[k4].x * inv, acc[k4].y * inv, acc[k4].z * inv, acc[k4].w * inv);
             }
             if (tid == 0) *counter = 0;
         }

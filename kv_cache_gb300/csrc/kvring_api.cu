@@ -142,7 +142,7 @@ int choose_splits(const kvring_t* r, int units, int ntiles) {
     int best = 1;
     long long best_cost = -1;
     const long long slots = (long long)r->num_sms;   // one attention CTA per SM
-    for (int s = 1; s <= std::min(r->max_splits, ntiles); ++s) {
+    for (int s = 1; s <= std::min(std::min(r->max_splits, 4), ntiles); ++s) {   // at most 4 (the merge's limit)
         const int tps = (ntiles + s - 1) / s;
         const int se = (ntiles + tps - 1) / tps;
         const long long waves = ((long long)units * se + slots - 1) / slots;
