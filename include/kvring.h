@@ -176,7 +176,8 @@ int kvring_debug_fault(kvring_t* ring, int32_t skip_tile, int64_t timeout_ns);
  *   q_bf16: [n_q][H][d]; query i sits at position q_pos0 + i
  *   out_f32: [n_q][H][d]
  * Slots [0, count) are attended; slots_padded is a multiple of 128 and the pad
- * slots' V codes must be finite (zero).  k8, vt8, q and out are 16-byte aligned.
+ * slots' V codes must be finite (zero).  k8, vt8, kamax, vamax, q and out are
+ * 16-byte aligned.
  * err_word: 4 ints, set to KVRING_ETIMEOUT (and kernel, wait site, block) if a
  * bounded device wait runs out; NULL leaves such time-outs unreported.
  *

@@ -110,7 +110,9 @@ struct AttendSmem {
     static constexpr int offK = offQ + 2 * kQ;
     static constexpr int offV = offK + kStages * kK;
     static constexpr int offV16 = offV + kStages * kV;
-    static constexpr int offBar = offV16 + 2 * kV16;
+    static constexpr int kAm = 2 * 128 * 4;        // the tile's K and V chunk amax rows (fp32)
+    static constexpr int offAm = offV16 + 2 * kV16;
+    static constexpr int offBar = offAm + kStages * kAm;
     static constexpr int kBars = 18;
     static constexpr int offMisc = offBar + kBars * 8;
     static constexpr int kBytes = offMisc + 64;
@@ -200,6 +202,150 @@ __device__ __forceinline__ float rcp_approx(float x) {
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
+constexpr float kInv448 = 1.f / 448.f;
+
+// Largest of 32 raw scores.
+__device__ __forceinline__ float max32(const uint32_t (&r)[32]) {
+    float m0 = fmax3(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]));
+    float m1 = fmax3(__uint_as_float(r[3]), __uint_as_float(r[4]), __uint_as_float(r[5]));
+    float m2 = fmax3(__uint_as_float(r[6]), __uint_as_float(r[7]), __uint_as_float(r[8]));
+    float m3 = fmax3(__uint_as_float(r[9]), __uint_as_float(r[10]), __uint_as_float(r[11]));
+#pragma unroll
+    for (int e = 12; e < 28; e += 8) {
+        m0 = fmax3(m0, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+        m1 = fmax3(m1, __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+        m2 = fmax3(m2, __uint_as_float(r[e + 4]), __uint_as_float(r[e + 5]));
+        m3 = fmax3(m3, __uint_as_float(r[e + 6]), __uint_as_float(r[e + 7]));
+    }
+    m0 = fmax3(m0, __uint_as_float(r[28]), __uint_as_float(r[29]));
+    m1 = fmax3(m1, __uint_as_float(r[30]), __uint_as_float(r[31]));
+    return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+}
+
+// One-range group: P = 2^(raw * c1 + c0) packed as fp16 pairs.  Returns the
+// group's share of the row sum, (sum of the fp32 P + fp16 rounding of the
+// largest one) * inv_sv; graw is the group's largest raw score.
+__device__ __forceinline__ float p_one_range(const uint32_t (&r)[32], float c1, float c0, float graw, float inv_sv,
+                                             uint32_t (&pk)[16]) {
+    const float2 c1v = make_float2(c1, c1), c0v = make_float2(c0, c0);
+    float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+        const float2 x01 = ffma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c1v, c0v);
+        const float2 x23 = ffma2(make_float2(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])), c1v, c0v);
+        const float2 p01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
+        const float2 p23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
+        pk[e / 2] = h2_bits(__floats2half2_rn(p01.x, p01.y));
+        pk[e / 2 + 1] = h2_bits(__floats2half2_rn(p23.x, p23.y));
+        s0 = fadd2(s0, p01);
+        s1 = fadd2(s1, p23);
+    }
+    const float pm = ex2_approx(fmaf(graw, c1, c0));
+    const float corr = __half2float(__float2half_rn(pm)) - pm;
+    return ((s0.x + s0.y) + (s1.x + s1.y) + corr) * inv_sv;
+}
+
+// Scales of one 32-column group of a tile, for the general (not one-range) path.
+// Lane e's own column is 32g + e.  kind 0: one range; 1: range A = columns
+// [0, b), range B = [b, 32); 2: per-column scales.  k* already carry the row's a.
+struct GroupScales {
+    int kind, b;
+    float kA, lA, iA, kB, lB, iB;   // ks * a, lg2(sv), 1 / sv of ranges A and B
+    float ks, ls, is;               // ks, lg2(sv), 1 / sv of the lane's own column (no a)
+};
+
+__device__ __forceinline__ GroupScales group_scales(const float* am, int g, int slot0, int count, float a, int lane) {
+    GroupScales s;
+    const int col = g * 32 + lane;
+    const bool valid = slot0 + col < count;
+    const float ka = valid ? am[col] : -1.f;
+    const float va = valid ? am[128 + col] : -1.f;
+    const float sv = va == 0.f ? 1.f : va * kInv448;
+    s.ks = valid ? (ka == 0.f ? 1.f : ka * kInv448) : 0.f;
+    s.ls = valid ? lg2_approx(sv) : -INFINITY;
+    s.is = valid ? rcp_approx(sv) : 0.f;
+    const float ka0 = __shfl_sync(0xffffffffu, ka, 0);
+    const float va0 = __shfl_sync(0xffffffffu, va, 0);
+    const uint32_t diff = __ballot_sync(0xffffffffu, ka != ka0 || va != va0);
+    s.kind = 0;
+    s.b = 32;
+    if (diff) {
+        s.b = __ffs(diff) - 1;
+        const float kab = __shfl_sync(0xffffffffu, ka, s.b);
+        const float vab = __shfl_sync(0xffffffffu, va, s.b);
+        s.kind = __ballot_sync(0xffffffffu, lane >= s.b && (ka != kab || va != vab)) ? 2 : 1;
+    }
+    s.kA = __shfl_sync(0xffffffffu, s.ks, 0) * a;
+    s.lA = __shfl_sync(0xffffffffu, s.ls, 0);
+    s.iA = __shfl_sync(0xffffffffu, s.is, 0);
+    const int bs = s.b & 31;
+    s.kB = __shfl_sync(0xffffffffu, s.ks, bs) * a;
+    s.lB = __shfl_sync(0xffffffffu, s.ls, bs);
+    s.iB = __shfl_sync(0xffffffffu, s.is, bs);
+    return s;
+}
+
+// Row max of z = raw * ks * a + lg2(sv) over one group, general path.
+__device__ __forceinline__ float zmax_group(const uint32_t (&r)[32], const GroupScales& s, float a) {
+    if (s.kind == 0) return fmaf(max32(r), s.kA, s.lA);
+    float m = -INFINITY;
+    if (s.kind == 1) {
+        float mA = -INFINITY, mB = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const float x = __uint_as_float(r[e]);
+            mA = fmaxf(mA, e < s.b ? x : -INFINITY);
+            mB = fmaxf(mB, e < s.b ? -INFINITY : x);
+        }
+        return fmaxf(fmaf(mA, s.kA, s.lA), fmaf(mB, s.kB, s.lB));
+    }
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+        const float ksa = __shfl_sync(0xffffffffu, s.ks, e) * a;
+        const float ls = __shfl_sync(0xffffffffu, s.ls, e);
+        m = fmaxf(m, fmaf(__uint_as_float(r[e]), ksa, ls));
+    }
+    return m;
+}
+
+// P of one group, general path (kinds 1 and 2 sum the rounded P themselves).
+__device__ __forceinline__ float p_group(const uint32_t (&r)[32], const GroupScales& s, float M, float a,
+                                         uint32_t (&pk)[16]) {
+    if (s.kind == 0) return p_one_range(r, s.kA, s.lA - M, max32(r), s.iA, pk);
+    float lsum = 0.f;
+    if (s.kind == 1) {
+        const float c0A = s.lA - M, c0B = s.lB - M;
+        float sA = 0.f, sB = 0.f;
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+            const bool a0 = e < s.b, a1 = e + 1 < s.b;
+            const float p0 = ex2_approx(fmaf(__uint_as_float(r[e]), a0 ? s.kA : s.kB, a0 ? c0A : c0B));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(r[e + 1]), a1 ? s.kA : s.kB, a1 ? c0A : c0B));
+            const __half2 hv = __floats2half2_rn(p0, p1);
+            pk[e / 2] = h2_bits(hv);
+            const float2 back = __half22float2(hv);
+            sA += (a0 ? back.x : 0.f) + (a1 ? back.y : 0.f);
+            sB += (a0 ? 0.f : back.x) + (a1 ? 0.f : back.y);
+        }
+        return sA * s.iA + sB * s.iB;
+    }
+    // per-column scales (slots past the valid count have ks = 0, lg2 sv = -inf,
+    // hence P exactly 0; the exponent is capped so that 2^x stays finite)
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+        const float k0 = __shfl_sync(0xffffffffu, s.ks, e) * a, k1 = __shfl_sync(0xffffffffu, s.ks, e + 1) * a;
+        const float l0 = __shfl_sync(0xffffffffu, s.ls, e), l1 = __shfl_sync(0xffffffffu, s.ls, e + 1);
+        const float i0 = __shfl_sync(0xffffffffu, s.is, e), i1 = __shfl_sync(0xffffffffu, s.is, e + 1);
+        const float p0 = ex2_approx(fminf(fmaf(__uint_as_float(r[e]), k0, l0 - M), 64.f));
+        const float p1 = ex2_approx(fminf(fmaf(__uint_as_float(r[e + 1]), k1, l1 - M), 64.f));
+        const __half2 hv = __floats2half2_rn(p0, p1);
+        pk[e / 2] = h2_bits(hv);
+        const float2 back = __half22float2(hv);
+        lsum = fmaf(back.x, i0, fmaf(back.y, i1, lsum));
+    }
+    return lsum;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kAttendThreads, 1)
 attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ AttendMaps maps) {
@@ -211,11 +357,11 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
     uint8_t* sK = smem + L::offK;
     uint8_t* sV = smem + L::offV;
     uint8_t* sV16 = smem + L::offV16;
+    uint8_t* sAm = smem + L::offAm;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::offBar);
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + L::offMisc);
     volatile int* sAbort = reinterpret_cast<volatile int*>(smem + L::offMisc + 4);
     volatile int* sLast = reinterpret_cast<volatile int*>(smem + L::offMisc + 8);
-    float* sRed = reinterpret_cast<float*>(smem + L::offMisc + 16);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -235,35 +381,27 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
 
     if (warp == 0) tmem_alloc(sTmem, 512);
     if (tid == 0) {
-        const int counts[L::kBars] = {1, 1, 1, 1, 129, 129, 129, 1, 1, 128, 128, 1, 1, 128, 128, 1, 1, 1};
+        // A stage is free again after the issuer's commit (its S MMAs are done), the
+        // 128 converter threads (its V tile is widened) and one arrival per softmax
+        // warp of each active query tile (they read its scale rows).
+        const int kve = 1 + 128 + 4 * nq;
+        const int counts[L::kBars] = {1, 1, 1, 1, kve, kve, kve, 1, 1, 128, 128, 1, 1, 128, 128, 1, 1, 1};
         for (int b = 0; b < L::kBars; ++b) mbar_init(&bars[b], counts[b]);
         fence_mbar_init();
         *sAbort = 0;
         *sLast = 0;
     }
-    // V scale reference of this split: largest V scale among its valid slots
-    if (warp >= 8 && warp < 12) {
-        const int c = tid - 256;
-        const int s_end = min((j0 + nt) * 128, p.count);
-        float m = 0.f;
-        for (int s = j0 * 128 + c; s < s_end; s += 128) m = fmaxf(m, scale_of(__ldg(vam + s)));
-#pragma unroll
-        for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-        if (lane == 0) sRed[warp - 8] = m;
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *sTmem;
-    const float sv_ref = fmaxf(fmaxf(sRed[0], sRed[1]), fmaxf(sRed[2], sRed[3]));
-    const float inv_sv_ref = __frcp_rn(sv_ref);
 
     // softmax state (warps 0-7), kept for the epilogue
     const int q = warp >> 2;
     const int wq = warp & 3;
     const int row = tid & 127;
     const int qrow = (2 * pair + q) * 128 + row;
-    float m_run = -INFINITY, l_run = 0.f, a = 0.f;
+    float M = -INFINITY, l_run = 0.f;
     // producer state (warp 12, lane 0)
     int issued[NST];
 #pragma unroll
@@ -282,100 +420,85 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
 
     if (warp < 8) {
         // ------------------------------------------------------------ softmax
+        // Weights in log2 units: slot c of row t has z = S[t][c] * ks_c * a_t + lg2(sv_c)
+        // with a_t = (Q scale of the row) * log2(e) / sqrt(d), ks / sv the slot's K / V
+        // scales.  The V scale rides in the exponent, so P = 2^(z - M) is the weight
+        // already multiplied by the V scale (O += P V8 then sums w * sv * v8), and the
+        // row sum takes it out again with 1/sv.  M is a lazy running max of z.
         const bool active = q < nq;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t tS = tmem + 128 * q + lane_off;
         const uint32_t tO = tmem + 256 + 128 * q + lane_off;
-        a = scale_of(__ldg(p.qamax + (size_t)h * p.Tstride + qrow)) * p.log2e_rsqrt_d;
-        // Per-slot scales of a tile, held by the warp: lane e has columns e, 32+e,
-        // 64+e, 96+e (one per 32-column group).  The next tile's amax values are
-        // loaded while the current tile is processed.
-        float kan[4], van[4];
-        auto load_amax = [&](int it2) {
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                const int s = (j0 + it2) * 128 + g * 32 + lane;
-                const bool v = it2 < nt && s < p.count;
-                kan[g] = v ? __ldg(kam + s) : -1.f;
-                van[g] = v ? __ldg(vam + s) : -1.f;
-            }
-        };
-        if (active) load_amax(0);
+        const float a = scale_of(__ldg(p.qamax + (size_t)h * p.Tstride + qrow)) * p.log2e_rsqrt_d;
         for (int it = 0; active && it < nt; ++it) {
-            const int nvalid = min(128, p.count - (j0 + it) * 128);
-            // this tile's scales: k scale, V ratio and its reciprocal per column, and
-            // per group whether all 32 columns are valid and share one pair
-            // (amax * (1/448) is within one fp32 rounding of amax / 448, which is all
-            // the attention needs; amax == 0 means scale 1)
-            float ksv[4], rrv[4], riv[4], gks[4], glg[4], gri[4];
-            bool uni[4];
+            const int st = it % NST;
+            const int slot0 = (j0 + it) * 128;
+            const float* am = reinterpret_cast<const float*>(sAm + st * L::kAm);   // K amax [128], V amax [128]
+            if (!warp_wait(&bars[kBKVF + st], (uint32_t)((it / NST) & 1), sAbort, p, kWaitKVFull)) break;
+            // Tile setup.  The columns of one chunk share one pair of scales, so a
+            // 32-column group is usually one range; a tile whose four groups all are
+            // (the common case) takes the fast path below with the scales of each
+            // group's first column, derived by lane g for group g.  (amax * (1/448) is
+            // within one fp32 rounding of amax / 448, which is all the attention
+            // needs; amax == 0 means scale 1.)
+            float gk[4], gl[4], gi[4];
+            bool uni;
+            {
+                const int gcol = (lane & 3) * 32;
+                const bool gvalid = slot0 + gcol < p.count;
+                const float gka = am[gcol], gva = am[128 + gcol];
+                const float sv = gva == 0.f ? 1.f : gva * kInv448;
+                const float ks = gvalid ? (gka == 0.f ? 1.f : gka * kInv448) : 0.f;
+                const float ls = gvalid ? lg2_approx(sv) : -INFINITY;
+                const float is = gvalid ? rcp_approx(sv) : 0.f;
+                bool same = true;
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                const bool valid = kan[g] >= 0.f;
-                constexpr float k1_448 = 1.f / 448.f;
-                ksv[g] = valid ? (kan[g] == 0.f ? 1.f : kan[g] * k1_448) : 0.f;
-                rrv[g] = valid ? (van[g] == 0.f ? 1.f : van[g] * k1_448) * inv_sv_ref : 0.f;
-                riv[g] = valid ? rcp_approx(rrv[g]) : 0.f;
-                gks[g] = __shfl_sync(0xffffffffu, ksv[g], 0);
-                const float r0 = __shfl_sync(0xffffffffu, rrv[g], 0);
-                uni[g] = __all_sync(0xffffffffu, valid && ksv[g] == gks[g] && rrv[g] == r0);
-                glg[g] = uni[g] ? lg2_approx(r0) : 0.f;
-                gri[g] = __shfl_sync(0xffffffffu, riv[g], 0);
+                for (int g = 0; g < 4; ++g) {
+                    gk[g] = __shfl_sync(0xffffffffu, ks, g) * a;   // a is this thread's own row's
+                    gl[g] = __shfl_sync(0xffffffffu, ls, g);
+                    gi[g] = __shfl_sync(0xffffffffu, is, g);
+                    const bool v0 = slot0 + g * 32 < p.count;
+                    const bool v = slot0 + g * 32 + lane < p.count;
+                    same = same && v == v0 &&
+                           (!v || (am[g * 32 + lane] == am[g * 32] && am[128 + g * 32 + lane] == am[128 + g * 32]));
+                }
+                uni = __all_sync(0xffffffffu, same);
             }
-            load_amax(it + 1);
             if (!warp_wait(&bars[kBSF + q], (uint32_t)(it & 1), sAbort, p, kWaitS)) break;
             tc_fence_after();
-            // pass 1: row max of raw * k_scale (two groups per tensor-memory wait);
-            // per uniform group also its largest raw value
-            float tm = -INFINITY;
-            float graw[4];
+            // pass 1: row max of z over the tile
+            float tz = -INFINITY;
+            float gm[4];
+            if (uni) {
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t ra[32], rb[32];
-                tmem_ld32_async(tS + hh * 64, ra);
-                tmem_ld32_async(tS + hh * 64 + 32, rb);
-                tmem_wait_ld_dep(ra);
-                tmem_dep(rb);
-#pragma unroll
-                for (int k2 = 0; k2 < 2; ++k2) {
-                    const int g = hh * 2 + k2;
-                    const uint32_t* r = k2 == 0 ? ra : rb;
-                    if (uni[g]) {
-                        float m0 = fmax3(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]));
-                        float m1 = fmax3(__uint_as_float(r[3]), __uint_as_float(r[4]), __uint_as_float(r[5]));
-                        float m2 = fmax3(__uint_as_float(r[6]), __uint_as_float(r[7]), __uint_as_float(r[8]));
-                        float m3 = fmax3(__uint_as_float(r[9]), __uint_as_float(r[10]), __uint_as_float(r[11]));
-#pragma unroll
-                        for (int e = 12; e < 28; e += 8) {
-                            m0 = fmax3(m0, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
-                            m1 = fmax3(m1, __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
-                            m2 = fmax3(m2, __uint_as_float(r[e + 4]), __uint_as_float(r[e + 5]));
-                            m3 = fmax3(m3, __uint_as_float(r[e + 6]), __uint_as_float(r[e + 7]));
-                        }
-                        m0 = fmax3(m0, __uint_as_float(r[28]), __uint_as_float(r[29]));
-                        m1 = fmax3(m1, __uint_as_float(r[30]), __uint_as_float(r[31]));
-                        graw[g] = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-                        tm = fmaxf(tm, graw[g] * gks[g]);
-                    } else {
-                        graw[g] = 0.f;
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const float ks = __shfl_sync(0xffffffffu, ksv[g], e);
-                            if (g * 32 + e < nvalid) tm = fmaxf(tm, __uint_as_float(r[e]) * ks);
-                        }
-                    }
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t ra[32], rb[32];
+                    tmem_ld32_async(tS + hh * 64, ra);
+                    tmem_ld32_async(tS + hh * 64 + 32, rb);
+                    tmem_wait_ld_dep(ra);
+                    tmem_dep(rb);
+                    gm[2 * hh] = max32(ra);
+                    gm[2 * hh + 1] = max32(rb);
+                    tz = fmaxf(tz, fmaxf(fmaf(gm[2 * hh], gk[2 * hh], gl[2 * hh]), fmaf(gm[2 * hh + 1], gk[2 * hh + 1], gl[2 * hh + 1])));
+                }
+            } else {
+#pragma unroll 1
+                for (int g = 0; g < 4; ++g) {
+                    uint32_t r[32];
+                    tmem_ld32(tS + g * 32, r);
+                    tz = fmaxf(tz, zmax_group(r, group_scales(am, g, slot0, p.count, a, lane), a));
                 }
             }
-            // Lazy running max: moved only when the row max grows by more than 2^15
-            // (so P stays below 2^15 < 65504, finite in fp16); then O and the row sum
-            // are rescaled.  Tensor-memory access is warp-collective.  O_q is stable
-            // here: S_q(j) was issued behind O_q += P_q(j-1) V and has completed.
-            const bool first = m_run == -INFINITY;
-            const bool grow = !first && (tm - m_run) * a > 15.f;
+            // Lazy running max: moved only when the row max grows by more than 15 (so
+            // P stays below 2^15 < 65504, finite in fp16); then O and the row sum are
+            // rescaled.  Tensor-memory access is warp-collective.  O_q is stable here:
+            // S_q(j) was issued behind O_q += P_q(j-1) V and has completed.
+            const bool first = M == -INFINITY;
+            const bool grow = !first && tz - M > 15.f;
             if (__any_sync(0xffffffffu, grow)) {
-                const float alpha = grow ? ex2_approx((m_run - tm) * a) : 1.f;
+                const float alpha = grow ? ex2_approx(M - tz) : 1.f;
                 if (it > 0) {
-#pragma unroll
+#pragma unroll 1
                     for (int cc = 0; cc < D / 32; ++cc) {
                         uint32_t o[32];
                         tmem_ld32(tO + cc * 32, o);
@@ -386,71 +509,46 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                 }
                 l_run *= alpha;
             }
-            if (first || grow) m_run = tm;
-            const float ma = m_run * a;
-            // pass 2: P = 2^(x - m) * (V scale ratio) as fp16, over S in tensor memory.
-            // The row sum must use the same (rounded) weights that O += P V sees
-            // wherever one weight dominates: it sums the fp32 P and adds back the fp16
-            // rounding of each group's largest element (the row's dominant weight is
-            // always one of them); the other elements' rounding is at most 2^-12 of
-            // their own, non-dominant, share.
+            if (first || grow) M = tz;
+            // pass 2: P = 2^(z - M) as fp16, written over S in tensor memory (group g
+            // to columns [16g, 16g + 16), which hold only groups already read).  The
+            // row sum must use the same (rounded) weights that O += P V sees wherever
+            // one weight dominates: a one-range group sums the fp32 P and adds back
+            // the fp16 rounding of its largest element (the row's dominant weight is
+            // always one of them; the other elements' rounding is at most 2^-12 of
+            // their own, non-dominant, share); the other kinds sum the rounded values.
             float lsum = 0.f;
-            uint32_t r[32], rn[32];
-            tmem_ld32(tS, r);
+            if (uni) {
+                uint32_t r[32], rn[32];
+                tmem_ld32(tS, r);
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                if (g < 3) tmem_ld32_async(tS + (g + 1) * 32, rn);
-                uint32_t pk[16];
-                if (uni[g]) {
-                    const float c1 = gks[g] * a;
-                    const float c0 = glg[g] - ma;
-                    const float2 c1v = make_float2(c1, c1), c0v = make_float2(c0, c0);
-                    float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
+                for (int g = 0; g < 4; ++g) {
+                    if (g < 3) tmem_ld32_async(tS + (g + 1) * 32, rn);
+                    uint32_t pk[16];
+                    lsum += p_one_range(r, gk[g], gl[g] - M, gm[g], gi[g], pk);
+                    tmem_st16(tS + g * 16, pk);
+                    if (g < 3) {
+                        tmem_wait_ld_dep(rn);
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        const float2 x01 = ffma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c1v, c0v);
-                        const float2 x23 = ffma2(make_float2(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])), c1v, c0v);
-                        const float2 p01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
-                        const float2 p23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
-                        pk[e / 2] = h2_bits(__floats2half2_rn(p01.x, p01.y));
-                        pk[e / 2 + 1] = h2_bits(__floats2half2_rn(p23.x, p23.y));
-                        s0 = fadd2(s0, p01);
-                        s1 = fadd2(s1, p23);
-                    }
-                    const float pm = ex2_approx(fmaf(graw[g], c1, c0));
-                    const float corr = __half2float(__float2half_rn(pm)) - pm;
-                    lsum += ((s0.x + s0.y) + (s1.x + s1.y) + corr) * gri[g];
-                } else {
-                    // columns of two chunks, or past the valid slots: per-column scales
-                    // (V ratio 0 beyond the valid slots, so those P are exactly 0; the
-                    // exponent is capped at 64 so that 2^x stays finite there)
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const float ks0 = __shfl_sync(0xffffffffu, ksv[g], e);
-                        const float ks1 = __shfl_sync(0xffffffffu, ksv[g], e + 1);
-                        const float r0 = __shfl_sync(0xffffffffu, rrv[g], e);
-                        const float r1 = __shfl_sync(0xffffffffu, rrv[g], e + 1);
-                        const float i0 = __shfl_sync(0xffffffffu, riv[g], e);
-                        const float i1 = __shfl_sync(0xffffffffu, riv[g], e + 1);
-                        const float p0 = ex2_approx(fminf(fmaf(__uint_as_float(r[e]) * ks0, a, -ma), 64.f)) * r0;
-                        const float p1 = ex2_approx(fminf(fmaf(__uint_as_float(r[e + 1]) * ks1, a, -ma), 64.f)) * r1;
-                        const __half2 hv = __floats2half2_rn(p0, p1);
-                        pk[e / 2] = h2_bits(hv);
-                        const float2 back = __half22float2(hv);
-                        lsum = fmaf(back.x, i0, fmaf(back.y, i1, lsum));
+                        for (int e = 0; e < 32; ++e) r[e] = rn[e];
                     }
                 }
-                tmem_st16(tS + g * 16, pk);     // P group g -> columns [16g, 16g + 16) of S_q
-                if (g < 3) {
-                    tmem_wait_ld_dep(rn);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = rn[e];
+            } else {
+#pragma unroll 1
+                for (int g = 0; g < 4; ++g) {
+                    uint32_t r[32], pk[16];
+                    tmem_ld32(tS + g * 32, r);
+                    lsum += p_group(r, group_scales(am, g, slot0, p.count, a, lane), M, a, pk);
+                    tmem_st16(tS + g * 16, pk);
                 }
             }
             l_run += lsum;
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&bars[kBPF + q]);
+            // the stage's scale rows are no longer needed
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kBKVE + st]);
         }
         if (active && !*sAbort) {
             // O_q is complete once the last O_q += P_q V has finished (its commit is
@@ -509,9 +607,11 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                 break;
             const int j = j0 + it;
             if (lane == 0 && j != p.skip_tile) {
-                mbar_expect_tx(&bars[kBKVF + st], (uint32_t)(L::kK + L::kV));
+                mbar_expect_tx(&bars[kBKVF + st], (uint32_t)(L::kK + L::kV + L::kAm));
                 tma_load_3d(sK + st * L::kK, &maps.k8, &bars[kBKVF + st], 0, j * 128, zrow);
                 tma_load_3d(sV + st * L::kV, &maps.vt8, &bars[kBKVF + st], j * 128, 0, zrow);
+                bulk_g2s(sAm + st * L::kAm, kam + (size_t)j * 128, 512, &bars[kBKVF + st]);
+                bulk_g2s(sAm + st * L::kAm + 512, vam + (size_t)j * 128, 512, &bars[kBKVF + st]);
                 issued[st]++;
             }
             __syncwarp();
@@ -597,7 +697,7 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
         const uint32_t tO = tmem + 256 + 128 * q + ((uint32_t)(wq * 32) << 16);
         const bool store = qrow < p.T;
         const bool direct = p.splits == 1;
-        const float f = direct ? 256.f * sv_ref / l_run : 256.f * sv_ref;   // V was widened as V * 2^-8
+        const float f = direct ? 256.f / l_run : 256.f;   // V was widened as V * 2^-8
         const size_t prow_i = ((size_t)split * p.H + h) * p.Tstride + qrow;
         float* dst = direct ? p.out + ((size_t)qrow * p.H + h) * D : p.part_o + prow_i * D;
 #pragma unroll
@@ -612,7 +712,7 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                                     __uint_as_float(r[e + 2]) * f, __uint_as_float(r[e + 3]) * f);
             }
         }
-        if (store && !direct) *reinterpret_cast<float2*>(p.part_ml + prow_i * 2) = make_float2(m_run * a, l_run);
+        if (store && !direct) *reinterpret_cast<float2*>(p.part_ml + prow_i * 2) = make_float2(M, l_run);
     }
     if (p.splits > 1) {
         // Split merge.  Every CTA counts itself in, aborted or not, so the

@@ -90,8 +90,8 @@ extern "C" int kvring_attend_noalloc(const void* k8, const void* vt8, const floa
                                                " exceeds the fixed scratch of " + std::to_string(kNoAllocMaxRows) +
                                                " rows; use kvring_attend or split the heads");
     if (!aligned(k8, 16) || !aligned(vt8, 16) || !aligned(q_bf16, 16) || !aligned(out_f32, 16) ||
-        !aligned(kamax, 4) || !aligned(vamax, 4) || !aligned(rope, 8) || (err_word && !aligned(err_word, 4)))
-        return noalloc_fail(KVRING_EINVAL, "k8, vt8, q and out must be 16-byte aligned (rope 8, amax 4)");
+        !aligned(kamax, 16) || !aligned(vamax, 16) || !aligned(rope, 8) || (err_word && !aligned(err_word, 4)))
+        return noalloc_fail(KVRING_EINVAL, "k8, vt8, kamax, vamax, q and out must be 16-byte aligned (rope 8)");
 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
