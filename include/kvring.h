@@ -175,9 +175,10 @@ int kvring_debug_fault(kvring_t* ring, int32_t skip_tile, int64_t timeout_ns);
  *          cosine in float64, w_i = theta^(-2i/d) (the table kvring_create builds)
  *   q_bf16: [n_q][H][d]; query i sits at position q_pos0 + i
  *   out_f32: [n_q][H][d]
- * Slots [0, count) are attended; slots_padded is a multiple of 128 and the pad
- * slots' V codes must be finite (zero).  k8, vt8, kamax, vamax, q and out are
- * 16-byte aligned.
+ * Slots [0, count) are attended; slots_padded is a multiple of 128 and the K
+ * and V codes of slots [count, slots_padded) must be finite (zero will do): they
+ * get weight exactly 0, but 0 times a NaN code is not 0.  k8, vt8, kamax,
+ * vamax, q and out are 16-byte aligned.
  * err_word: 4 ints, set to KVRING_ETIMEOUT (and kernel, wait site, block) if a
  * bounded device wait runs out; NULL leaves such time-outs unreported.
  *

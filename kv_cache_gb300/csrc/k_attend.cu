@@ -1,4 +1,4 @@
-// K3 (Q prep), K4 (FP8 attention over the ring) and K5 (split combine).
+// K3 (Q prep) and K4 (FP8 attention over the ring, with the KV-split merge).
 //
 // The pages have every attention call read a cache of 5,788 slots of which 757
 // are new, 240 calls per step (wechild.cn news item on Runway's real-time
@@ -8,17 +8,19 @@
 // attention kernel that accepts per-head scales (same article, section "Latenza
 // dei turni e altre configurazioni GPU").
 //
-// K4 is one CTA of 128 threads per (head, 128-row query tile, KV split):
-//  * Q (e4m3, from K3), K tiles [128 slots][d] and V tiles [d][128 slots] (e4m3)
-//    arrive by TMA into 128-byte-swizzled shared memory, two K/V stages deep.
-//  * S = Q K^T runs on tcgen05 (kind::f8f6f4, M = N = 128) into tensor memory.
-//  * Thread i owns query row i (tensor-memory lane i): it reads S, applies the
-//    per-slot K scale, keeps a running max m and sum l (online softmax; the max
-//    is only moved when it grows by more than 2^15, so O is rarely rescaled),
-//    and writes P = 2^(x - m) * (V scale of the slot / V scale reference) as
-//    fp16 into shared memory.
-//  * The V tile is widened from e4m3 to fp16 in shared memory (exact), and
-//    O += P V runs on tcgen05 (kind::f16, M = 128, N = d) into tensor memory.
+// K4 is one CTA of 16 warps per (head, pair of 128-row query tiles, KV split):
+//  * Q (e4m3, from K3), K tiles [128 slots][d], V tiles [d][128 slots] (e4m3) and
+//    the tile's K/V chunk amax rows arrive by TMA into shared memory, 3 stages.
+//  * S = Q K^T runs on tcgen05 (kind::f8f6f4, M = 128, N = 64 per half tile)
+//    into tensor memory, two S buffers per query tile.
+//  * Thread i of a softmax warp group owns query row i (tensor-memory lane i):
+//    the weight of slot c is 2^z with z = S * ks_c * a + lg2(sv_c) (K and V scale
+//    of the slot's chunk, a = Q scale of the row * log2(e) / sqrt(d)).  A first
+//    pass over the split's slots finds the exact row max M of z; the second
+//    writes P = 2^(z - M) <= 1 as fp16 over S and sums l = sum P / sv.
+//  * The V tile is widened from e4m3 to fp16 in shared memory (exact, as
+//    V * 2^-8) and O += P V runs on tcgen05 (kind::f16, M = 128, N = d, P from
+//    tensor memory); out = 2^8 O / l, or (2^8 O, M, l) per split for the merge.
 //  * Slots are walked in physical order 0..count-1: softmax attention does not
 //    depend on key order and each slot already carries its rotation, so the
 //    ring wrap needs no special case and no gather.
@@ -28,6 +30,7 @@
 #include "common.cuh"
 #include "kvring_internal.h"
 #include "tc.cuh"
+
 
 namespace kvring_impl {
 
@@ -86,19 +89,21 @@ cudaError_t launch_qprep(const QPrepParams& p, cudaStream_t s) {
 // One CTA of 16 warps per (head, pair of 128-row query tiles, KV split):
 //   warps 0-3   softmax for query tile 0 (tensor-memory lanes 0-127 of S0, O0)
 //   warps 4-7   softmax for query tile 1 (S1, O1)
-//   warps 8-11  V e4m3 -> fp16 per tile (bit operations, giving V * 2^-8 exactly)
-//   warp 12     TMA producer (the query tiles once, then K/V tiles, 3 stages)
-//   warp 13     tcgen05 issuer
-//   warps 14-15 idle (they keep two softmax warps and two others on every SM
+//   warps 8-11  per stage: the scale summaries of its four 32-column groups; in
+//               the second pass also V e4m3 -> fp16 (bit operations, V * 2^-8)
+//   warp 12     TMA producer (the query tiles once, then the split's tiles
+//               twice: K for the first pass, K and V for the second)
+//   warps 13-14 tcgen05 issuers, one per query tile
+//   warp 15     idle (it keeps two softmax warps and two others on every SM
 //               sub-partition, which the register split needs)
-// Tensor memory (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [384,384+d).
-// The softmax reads its S row once, writes P as packed fp16 back over the first
-// 64 columns of S, and O_q += P_q V runs with A in tensor memory.  The issuer
-// puts S_q(j+1) right behind O_q += P_q(j) V_j in the tensor pipe, so when a
-// softmax group sees S_q(j+1) its previous product is done: O_q can be rescaled
-// and P_q rewritten without another wait.  The two query tiles share every K/V
-// tile and alternate on the tensor pipe.  Hand-offs are mbarriers; every wait
-// is bounded and gives up as soon as another warp has recorded a time-out.
+// Tensor memory (512 columns): per query tile q two S buffers of 64 columns,
+// [128q, 128q + 64) and [128q + 64, 128q + 128), then O0 [256, 256 + d) and
+// O1 [384, 384 + d).  A 128-slot tile is worked as two halves, half u in S
+// buffer u % 2: while the softmax works on one half, S of the next is already
+// in the other buffer.  In the second pass the issuer puts S_q(u + 2) right
+// behind O_q += P_q(u) V in the tensor pipe, so S never overwrites P before it
+// is read.  Hand-offs are mbarriers; every wait is bounded and gives up as soon
+// as another warp has recorded a time-out.
 template <int D>
 struct AttendSmem {
     static constexpr int kStages = 3;
@@ -110,31 +115,35 @@ struct AttendSmem {
     static constexpr int offK = offQ + 2 * kQ;
     static constexpr int offV = offK + kStages * kK;
     static constexpr int offV16 = offV + kStages * kV;
-    static constexpr int kAm = 2 * 128 * 4;        // the tile's K and V chunk amax rows (fp32)
+    // the tile's K and V chunk amax rows (fp32, 512 bytes each), then the four
+    // groups' scale summaries (GroupInfo, 32 bytes each)
+    static constexpr int kAmRows = 2 * 128 * 4;
+    static constexpr int kAm = kAmRows + 4 * 32;
     static constexpr int offAm = offV16 + 2 * kV16;
     static constexpr int offBar = offAm + kStages * kAm;
-    static constexpr int kBars = 18;
+    static constexpr int kBars = 25;
     static constexpr int offMisc = offBar + kBars * 8;
     static constexpr int kBytes = offMisc + 64;
     static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
-// mbarrier slots
+// mbarrier slots ([q][b]: per query tile q and S buffer b, in that order)
 enum : int {
     kBQ = 0,        // query tiles landed (TMA)
-    kBKVF = 1,      // [3] K/V stage full (TMA)
-    kBKVE = 4,      // [3] K/V stage free: S MMAs done (commit) + 128 converter arrivals
-    kBSF = 7,       // [2] S_q computed, and the O_q += P_q V before it (commit)
-    kBPF = 9,       // [2] P_q in tensor memory (128 softmax arrivals)
-    kBOF = 11,      // [2] last O_q += P_q V done (commit)
-    kBVF = 13,      // [2] fp16 V buffer full (128 converter arrivals)
-    kBVE = 15,      // [2] fp16 V buffer free (commit after both PV MMAs)
-    kBDrain = 17,   // drain after an abort
+    kBKVF = 1,      // [3] stage full: K, V and the amax rows (TMA)
+    kBKVE = 4,      // [3] stage free: 128 converter arrivals + one per softmax warp (end of its tile)
+    kBSF = 7,       // [2][2] S_q half b computed (commit)
+    kBPF = 11,      // [2][2] first pass: S_q half b read out; second: P_q half b written (one arrival per softmax warp)
+    kBVF = 15,      // [2] fp16 V buffer full (128 converter arrivals)
+    kBVE = 17,      // [2] fp16 V buffer free (one commit per active issuer)
+    kBOF = 19,      // [2] O_q complete: the last O_q += P V (commit)
+    kBDrain = 21,   // drain after an abort (one commit per active issuer)
+    kBIF = 22,      // [3] the stage's group summaries written (one arrival per converter warp)
 };
 enum : int { kWaitQ = 1, kWaitKVFull = 2, kWaitKVEmpty = 3, kWaitS = 4, kWaitP = 5, kWaitO = 6, kWaitV16Full = 7,
              kWaitV16Empty = 8 };
 constexpr int kAttendThreads = 512;
-constexpr int kMaxSplits = 4;   // KV splits per (head, query pair); the merge keeps them all in registers
+constexpr int kMaxSplits = 4;   // KV splits per (head, query pair); the merge holds them all in registers
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -168,24 +177,24 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// S for one half tile: S[128 query rows][64 slots] = Q K_half^T, e4m3 operands in
+// shared memory (K-major rows of D bytes), fp32 accumulator in tensor memory.
 template <int D>
-__device__ __forceinline__ void issue_s(uint32_t tS, uint32_t aQ, uint32_t aK) {
-    constexpr uint32_t id = make_idesc(128, 128);
+__device__ __forceinline__ void issue_s_half(uint32_t tS, uint32_t aQ, uint32_t aK) {
+    constexpr uint32_t id = make_idesc(128, 64);
 #pragma unroll
     for (int k = 0; k < D / 32; ++k)
         mma_f8(tS, make_sdesc(aQ + k * 32, D), make_sdesc(aK + k * 32, D), id, k > 0 ? 1u : 0u);
 }
 
-// O += P V for one 128-slot tile: P (fp16) in tensor memory at tP, 8 columns per
-// 16-slot step; V fp16 in shared memory, 2 K-blocks of [D][64].
+// O += P V for one half tile (64 slots): P (fp16) in tensor memory at tP, 8 columns
+// per 16-slot step; V fp16 in shared memory, one K-block of [D][64].
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t aV16, bool accumulate) {
+__device__ __forceinline__ void issue_pv_half(uint32_t tO, uint32_t tP, uint32_t aV16blk, bool accumulate) {
     constexpr uint32_t id = make_idesc(128, D);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const uint32_t offv = (k >> 2) * (D * 128) + (k & 3) * 32;
-        mma_f16_ts(tO, tP + k * 8, make_sdesc(aV16 + offv, 128), id, (accumulate || k > 0) ? 1u : 0u);
-    }
+    for (int k = 0; k < 4; ++k)
+        mma_f16_ts(tO, tP + k * 8, make_sdesc(aV16blk + k * 32, 128), id, (accumulate || k > 0) ? 1u : 0u);
 }
 
 __device__ __forceinline__ float lg2_approx(float x) {
@@ -251,37 +260,80 @@ __device__ __forceinline__ float p_one_range(const uint32_t (&r)[32], float c1, 
 struct GroupScales {
     int kind, b;
     float kA, lA, iA, kB, lB, iB;   // ks * a, lg2(sv), 1 / sv of ranges A and B
-    float ks, ls, is;               // ks, lg2(sv), 1 / sv of the lane's own column (no a)
+    float ks, ls, is;               // ks, lg2(sv), 1 / sv of the lane's own column (kind 2 only)
 };
 
-__device__ __forceinline__ GroupScales group_scales(const float* am, int g, int slot0, int count, float a, int lane) {
-    GroupScales s;
-    const int col = g * 32 + lane;
-    const bool valid = slot0 + col < count;
-    const float ka = valid ? am[col] : -1.f;
-    const float va = valid ? am[128 + col] : -1.f;
+// Scale summary of one 32-column group of a tile, written once per tile by the
+// converter warps and read by all softmax warps.
+struct GroupInfo {
+    float ks, ls, is;      // range A: K scale, lg2(V scale), 1 / V scale (0, -inf, 0 past the valid slots)
+    int kind_b;            // kind | b << 8
+    float ksB, lsB, isB;   // range B
+    float pad;
+};
+
+// The K/V scales of column 32g + lane; ka / va are -1 past the valid slots.
+__device__ __forceinline__ void column_scales(const float* am, int col, bool valid, float& ka, float& va, float& ks,
+                                              float& ls, float& is) {
+    ka = valid ? am[col] : -1.f;
+    va = valid ? am[128 + col] : -1.f;
     const float sv = va == 0.f ? 1.f : va * kInv448;
-    s.ks = valid ? (ka == 0.f ? 1.f : ka * kInv448) : 0.f;
-    s.ls = valid ? lg2_approx(sv) : -INFINITY;
-    s.is = valid ? rcp_approx(sv) : 0.f;
+    ks = valid ? (ka == 0.f ? 1.f : ka * kInv448) : 0.f;
+    ls = valid ? lg2_approx(sv) : -INFINITY;
+    is = valid ? rcp_approx(sv) : 0.f;
+}
+
+// Builds the summary of group g (one warp, lane = column within the group); lane
+// 0 writes it.
+__device__ __forceinline__ void write_group_info(const float* am, int g, int slot0, int count, int lane,
+                                                 GroupInfo* out) {
+    const int col = g * 32 + lane;
+    float ka, va, ks, ls, is;
+    column_scales(am, col, slot0 + col < count, ka, va, ks, ls, is);
     const float ka0 = __shfl_sync(0xffffffffu, ka, 0);
     const float va0 = __shfl_sync(0xffffffffu, va, 0);
     const uint32_t diff = __ballot_sync(0xffffffffu, ka != ka0 || va != va0);
-    s.kind = 0;
-    s.b = 32;
+    int kind = 0, b = 32;
     if (diff) {
-        s.b = __ffs(diff) - 1;
-        const float kab = __shfl_sync(0xffffffffu, ka, s.b);
-        const float vab = __shfl_sync(0xffffffffu, va, s.b);
-        s.kind = __ballot_sync(0xffffffffu, lane >= s.b && (ka != kab || va != vab)) ? 2 : 1;
+        b = __ffs(diff) - 1;
+        const float kab = __shfl_sync(0xffffffffu, ka, b);
+        const float vab = __shfl_sync(0xffffffffu, va, b);
+        kind = __ballot_sync(0xffffffffu, lane >= b && (ka != kab || va != vab)) ? 2 : 1;
     }
-    s.kA = __shfl_sync(0xffffffffu, s.ks, 0) * a;
-    s.lA = __shfl_sync(0xffffffffu, s.ls, 0);
-    s.iA = __shfl_sync(0xffffffffu, s.is, 0);
-    const int bs = s.b & 31;
-    s.kB = __shfl_sync(0xffffffffu, s.ks, bs) * a;
-    s.lB = __shfl_sync(0xffffffffu, s.ls, bs);
-    s.iB = __shfl_sync(0xffffffffu, s.is, bs);
+    const float ksA = __shfl_sync(0xffffffffu, ks, 0), lsA = __shfl_sync(0xffffffffu, ls, 0);
+    const float isA = __shfl_sync(0xffffffffu, is, 0);
+    const int bs = b & 31;
+    const float ksB = __shfl_sync(0xffffffffu, ks, bs), lsB = __shfl_sync(0xffffffffu, ls, bs);
+    const float isB = __shfl_sync(0xffffffffu, is, bs);
+    if (lane == 0) {
+        float4* o = reinterpret_cast<float4*>(out);
+        o[0] = make_float4(ksA, lsA, isA, __int_as_float(kind | (b << 8)));
+        o[1] = make_float4(ksB, lsB, isB, 0.f);
+    }
+}
+
+// General-path scales of group g from its summary (and, for per-column groups,
+// from the amax rows).
+__device__ __forceinline__ GroupScales group_scales(const GroupInfo* info, const float* am, int g, int slot0,
+                                                    int count, float a, int lane) {
+    GroupScales s;
+    const float4 i0 = reinterpret_cast<const float4*>(info + g)[0];
+    const float4 i1 = reinterpret_cast<const float4*>(info + g)[1];
+    const int kb = __float_as_int(i0.w);
+    s.kind = kb & 3;
+    s.b = kb >> 8;
+    s.kA = i0.x * a;
+    s.lA = i0.y;
+    s.iA = i0.z;
+    s.kB = i1.x * a;
+    s.lB = i1.y;
+    s.iB = i1.z;
+    s.ks = s.ls = s.is = 0.f;
+    if (s.kind == 2) {
+        const int col = g * 32 + lane;
+        float ka, va;
+        column_scales(am, col, slot0 + col < count, ka, va, s.ks, s.ls, s.is);
+    }
     return s;
 }
 
@@ -381,11 +433,12 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
 
     if (warp == 0) tmem_alloc(sTmem, 512);
     if (tid == 0) {
-        // A stage is free again after the issuer's commit (its S MMAs are done), the
-        // 128 converter threads (its V tile is widened) and one arrival per softmax
-        // warp of each active query tile (they read its scale rows).
-        const int kve = 1 + 128 + 4 * nq;
-        const int counts[L::kBars] = {1, 1, 1, 1, kve, kve, kve, 1, 1, 128, 128, 1, 1, 128, 128, 1, 1, 1};
+        // A stage is free again after the 128 converter threads (its V tile is
+        // widened) and one arrival per softmax warp of each active query tile (at
+        // the end of its tile: its S MMAs are done and its scale rows read).
+        const int kve = 128 + 4 * nq;
+        const int counts[L::kBars] = {1, 1, 1, 1, kve, kve, kve, 1,  1,  1,  1, 4, 4,
+                                      4, 4, 128, 128, nq, nq, 1,  1,  nq, 4, 4, 4};
         for (int b = 0; b < L::kBars; ++b) mbar_init(&bars[b], counts[b]);
         fence_mbar_init();
         *sAbort = 0;
@@ -395,6 +448,8 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *sTmem;
+    const int nh = 2 * nt;   // half tiles of 64 slots in one pass over the split
+    const int nu = 2 * nh;   // both passes
 
     // softmax state (warps 0-7), kept for the epilogue
     const int q = warp >> 2;
@@ -410,12 +465,12 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
 
     // Register split.  The launch gives each of the 16 warps 128 registers per
     // thread, and every SM sub-partition (warps w, w+4, w+8, w+12) holds two
-    // softmax warps and two others; 2 x 184 + 2 x 72 = 2 x 128 + 2 x 128, so the
+    // softmax warps and two others; 2 x 176 + 2 x 80 = 2 x 128 + 2 x 128, so the
     // increase always fits in the registers its own sub-partition released.
     if (warp < 8) {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 184;" ::: "memory");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 176;" ::: "memory");
     } else {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
     }
 
     if (warp < 8) {
@@ -424,174 +479,162 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
         // with a_t = (Q scale of the row) * log2(e) / sqrt(d), ks / sv the slot's K / V
         // scales.  The V scale rides in the exponent, so P = 2^(z - M) is the weight
         // already multiplied by the V scale (O += P V8 then sums w * sv * v8), and the
-        // row sum takes it out again with 1/sv.  M is a lazy running max of z.
+        // row sum takes it out again with 1/sv.
+        // Two passes over the split's slots: the first computes S only and keeps the
+        // exact row max M of z; the second computes P = 2^(z - M) <= 1 and O += P V
+        // with M fixed, so O is never rescaled.  Each 128-slot tile is worked in two
+        // halves of 64, each with its own S buffer in tensor memory, so that S of the
+        // next half is computed while this one is worked on.
         const bool active = q < nq;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t tS = tmem + 128 * q + lane_off;
-        const uint32_t tO = tmem + 256 + 128 * q + lane_off;
         const float a = scale_of(__ldg(p.qamax + (size_t)h * p.Tstride + qrow)) * p.log2e_rsqrt_d;
-        for (int it = 0; active && it < nt; ++it) {
-            const int st = it % NST;
-            const int slot0 = (j0 + it) * 128;
-            const float* am = reinterpret_cast<const float*>(sAm + st * L::kAm);   // K amax [128], V amax [128]
-            if (!warp_wait(&bars[kBKVF + st], (uint32_t)((it / NST) & 1), sAbort, p, kWaitKVFull)) break;
-            // Tile setup.  The columns of one chunk share one pair of scales, so a
-            // 32-column group is usually one range; a tile whose four groups all are
-            // (the common case) takes the fast path below with the scales of each
-            // group's first column, derived by lane g for group g.  (amax * (1/448) is
-            // within one fp32 rounding of amax / 448, which is all the attention
-            // needs; amax == 0 means scale 1.)
-            float gk[4], gl[4], gi[4];
-            bool uni;
-            {
-                const int gcol = (lane & 3) * 32;
-                const bool gvalid = slot0 + gcol < p.count;
-                const float gka = am[gcol], gva = am[128 + gcol];
-                const float sv = gva == 0.f ? 1.f : gva * kInv448;
-                const float ks = gvalid ? (gka == 0.f ? 1.f : gka * kInv448) : 0.f;
-                const float ls = gvalid ? lg2_approx(sv) : -INFINITY;
-                const float is = gvalid ? rcp_approx(sv) : 0.f;
-                bool same = true;
+        float gk[4], gl[4], gi[4];
+        bool uni[2];
+        const float* am = nullptr;
+        const GroupInfo* info = nullptr;
+        int slot0 = 0;
+        for (int u = 0; active && u < nu; ++u) {
+            const int ld = u >> 1, hb = u & 1, st = ld % NST;   // ld: the stage load this half reads
+            const bool main = u >= nh;
+            const uint32_t tSb = tS + 64 * hb;
+            if (hb == 0) {
+                slot0 = (j0 + ld % nt) * 128;
+                am = reinterpret_cast<const float*>(sAm + st * L::kAm);   // K amax [128], V amax [128]
+                info = reinterpret_cast<const GroupInfo*>(sAm + st * L::kAm + L::kAmRows);
+                // Tile setup from the converter's group summaries.  The columns of one
+                // chunk share one pair of scales, so a 32-column group is usually one
+                // range; a half whose two groups both are (the common case) takes the
+                // fast path below.
+                if (!warp_wait(&bars[kBIF + st], (uint32_t)((ld / NST) & 1), sAbort, p, kWaitKVFull)) break;
+                int kinds = 0;
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
-                    gk[g] = __shfl_sync(0xffffffffu, ks, g) * a;   // a is this thread's own row's
-                    gl[g] = __shfl_sync(0xffffffffu, ls, g);
-                    gi[g] = __shfl_sync(0xffffffffu, is, g);
-                    const bool v0 = slot0 + g * 32 < p.count;
-                    const bool v = slot0 + g * 32 + lane < p.count;
-                    same = same && v == v0 &&
-                           (!v || (am[g * 32 + lane] == am[g * 32] && am[128 + g * 32 + lane] == am[128 + g * 32]));
+                    const float4 i0 = reinterpret_cast<const float4*>(info + g)[0];
+                    gk[g] = i0.x * a;   // a is this thread's own row's
+                    gl[g] = i0.y;
+                    gi[g] = i0.z;
+                    kinds |= (__float_as_int(i0.w) & 3) << (8 * g);
                 }
-                uni = __all_sync(0xffffffffu, same);
+                uni[0] = (kinds & 0xFFFF) == 0;
+                uni[1] = (kinds >> 16) == 0;
             }
-            if (!warp_wait(&bars[kBSF + q], (uint32_t)(it & 1), sAbort, p, kWaitS)) break;
+            const bool un = hb == 0 ? uni[0] : uni[1];
+            const int g0 = 2 * hb;   // the half's groups are g0 and g0 + 1
+            if (!warp_wait(&bars[kBSF + 2 * q + hb], (uint32_t)(ld & 1), sAbort, p, kWaitS)) break;
             tc_fence_after();
-            // pass 1: row max of z over the tile
-            float tz = -INFINITY;
-            float gm[4];
-            if (uni) {
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t ra[32], rb[32];
-                    tmem_ld32_async(tS + hh * 64, ra);
-                    tmem_ld32_async(tS + hh * 64 + 32, rb);
-                    tmem_wait_ld_dep(ra);
-                    tmem_dep(rb);
-                    gm[2 * hh] = max32(ra);
-                    gm[2 * hh + 1] = max32(rb);
-                    tz = fmaxf(tz, fmaxf(fmaf(gm[2 * hh], gk[2 * hh], gl[2 * hh]), fmaf(gm[2 * hh + 1], gk[2 * hh + 1], gl[2 * hh + 1])));
+            // the half's S (two groups of 32 columns), read once into registers
+            uint32_t ra[32], rb[32];
+            tmem_ld32_async(tSb, ra);
+            tmem_ld32_async(tSb + 32, rb);
+            tmem_wait_ld_dep(ra);
+            tmem_dep(rb);
+            if (!main) {
+                // first pass: row max of z; the S buffer is free again once read
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kBPF + 2 * q + hb]);
+                float tz;
+                if (un) {
+                    tz = fmaxf(fmaf(max32(ra), hb ? gk[2] : gk[0], hb ? gl[2] : gl[0]),
+                               fmaf(max32(rb), hb ? gk[3] : gk[1], hb ? gl[3] : gl[1]));
+                } else {
+                    tz = fmaxf(zmax_group(ra, group_scales(info, am, g0, slot0, p.count, a, lane), a),
+                               zmax_group(rb, group_scales(info, am, g0 + 1, slot0, p.count, a, lane), a));
                 }
+                M = fmaxf(M, tz);
             } else {
-#pragma unroll 1
-                for (int g = 0; g < 4; ++g) {
-                    uint32_t r[32];
-                    tmem_ld32(tS + g * 32, r);
-                    tz = fmaxf(tz, zmax_group(r, group_scales(am, g, slot0, p.count, a, lane), a));
+                // second pass: P = 2^(z - M) as fp16, written over the half's S buffer
+                // (group g of the half to columns [16g, 16g + 16), which hold only
+                // values already read).  The row sum must use the same (rounded)
+                // weights that O += P V sees wherever one weight dominates: a one-range
+                // group sums the fp32 P and adds back the fp16 rounding of its largest
+                // element (the row's dominant weight is always one of them; the other
+                // elements' rounding is at most 2^-12 of their own, non-dominant,
+                // share); the other kinds sum the rounded values.
+                uint32_t pk[16];
+                float lsum;
+                if (un) {
+                    lsum = p_one_range(ra, hb ? gk[2] : gk[0], (hb ? gl[2] : gl[0]) - M, max32(ra), hb ? gi[2] : gi[0], pk);
+                } else {
+                    lsum = p_group(ra, group_scales(info, am, g0, slot0, p.count, a, lane), M, a, pk);
                 }
+                tmem_st16(tSb, pk);
+                if (un) {
+                    lsum += p_one_range(rb, hb ? gk[3] : gk[1], (hb ? gl[3] : gl[1]) - M, max32(rb), hb ? gi[3] : gi[1], pk);
+                } else {
+                    lsum += p_group(rb, group_scales(info, am, g0 + 1, slot0, p.count, a, lane), M, a, pk);
+                }
+                tmem_st16(tSb + 16, pk);
+                l_run += lsum;
+                // P_q(u) handed over once all 32 lanes' stores are done: one arrival per warp
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kBPF + 2 * q + hb]);
             }
-            // Lazy running max: moved only when the row max grows by more than 15 (so
-            // P stays below 2^15 < 65504, finite in fp16); then O and the row sum are
-            // rescaled.  Tensor-memory access is warp-collective.  O_q is stable here:
-            // S_q(j) was issued behind O_q += P_q(j-1) V and has completed.
-            const bool first = M == -INFINITY;
-            const bool grow = !first && tz - M > 15.f;
-            if (__any_sync(0xffffffffu, grow)) {
-                const float alpha = grow ? ex2_approx(M - tz) : 1.f;
-                if (it > 0) {
-#pragma unroll 1
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t o[32];
-                        tmem_ld32(tO + cc * 32, o);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(tO + cc * 32, o);
-                    }
-                }
-                l_run *= alpha;
+            if (hb == 1) {
+                // the end of the stage: its S MMAs are done and its scale rows read
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kBKVE + st]);
             }
-            if (first || grow) M = tz;
-            // pass 2: P = 2^(z - M) as fp16, written over S in tensor memory (group g
-            // to columns [16g, 16g + 16), which hold only groups already read).  The
-            // row sum must use the same (rounded) weights that O += P V sees wherever
-            // one weight dominates: a one-range group sums the fp32 P and adds back
-            // the fp16 rounding of its largest element (the row's dominant weight is
-            // always one of them; the other elements' rounding is at most 2^-12 of
-            // their own, non-dominant, share); the other kinds sum the rounded values.
-            float lsum = 0.f;
-            if (uni) {
-                uint32_t r[32], rn[32];
-                tmem_ld32(tS, r);
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    if (g < 3) tmem_ld32_async(tS + (g + 1) * 32, rn);
-                    uint32_t pk[16];
-                    lsum += p_one_range(r, gk[g], gl[g] - M, gm[g], gi[g], pk);
-                    tmem_st16(tS + g * 16, pk);
-                    if (g < 3) {
-                        tmem_wait_ld_dep(rn);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) r[e] = rn[e];
-                    }
-                }
-            } else {
-#pragma unroll 1
-                for (int g = 0; g < 4; ++g) {
-                    uint32_t r[32], pk[16];
-                    tmem_ld32(tS + g * 32, r);
-                    lsum += p_group(r, group_scales(am, g, slot0, p.count, a, lane), M, a, pk);
-                    tmem_st16(tS + g * 16, pk);
-                }
-            }
-            l_run += lsum;
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&bars[kBPF + q]);
-            // the stage's scale rows are no longer needed
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kBKVE + st]);
         }
         if (active && !*sAbort) {
-            // O_q is complete once the last O_q += P_q V has finished (its commit is
-            // the only arrival on this barrier)
+            // O_q is complete once the last O_q += P_q V has finished
             if (warp_wait(&bars[kBOF + q], 0u, sAbort, p, kWaitO)) tc_fence_after();
         }
     } else if (warp < 12) {
         // ------------------------------------------------------------ V e4m3 -> fp16
+        // Per stage load: each converter warp summarises the scales of one 32-column
+        // group (the softmax warps read the summaries); in the second pass the V tile
+        // is then widened into fp16 buffer j % 2, once both issuers have committed
+        // their last O += P V of tile j - 2.
         const int c0 = tid - 256;
-        for (int it = 0; it < nt; ++it) {
-            const int st = it % NST, b = it & 1;
-            if (it >= 2 && !warp_wait(&bars[kBVE + b], (uint32_t)(((it >> 1) - 1) & 1), sAbort, p, kWaitV16Empty))
-                break;
-            if (!warp_wait(&bars[kBKVF + st], (uint32_t)((it / NST) & 1), sAbort, p, kWaitKVFull)) break;
-            const uint8_t* src = sV + st * L::kV;
-            uint8_t* dst = sV16 + b * L::kV16;
+        for (int ld = 0; ld < 2 * nt; ++ld) {
+            const int st = ld % NST;
+            if (!warp_wait(&bars[kBKVF + st], (uint32_t)((ld / NST) & 1), sAbort, p, kWaitKVFull)) break;
+            write_group_info(reinterpret_cast<const float*>(sAm + st * L::kAm), warp - 8, (j0 + ld % nt) * 128, p.count,
+                             lane, reinterpret_cast<GroupInfo*>(sAm + st * L::kAm + L::kAmRows) + (warp - 8));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kBIF + st]);
+            if (ld >= nt) {
+                const int it = ld - nt, b = it & 1;
+                if (it >= 2 && !warp_wait(&bars[kBVE + b], (uint32_t)(((it >> 1) - 1) & 1), sAbort, p, kWaitV16Empty))
+                    break;
+                const uint8_t* src = sV + st * L::kV;
+                uint8_t* dst = sV16 + b * L::kV16;
 #pragma unroll
-            for (int qq = c0; qq < D * 8; qq += 128) {
-                const int dd = qq >> 3, c = qq & 7;
-                const uint4 w = *reinterpret_cast<const uint4*>(src + dd * 128 + ((c ^ (dd & 7)) << 4));
-                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-                // e4m3 -> fp16 with integer operations: sign to bit 15, the other 7 bits
-                // to bits 7-13, which is the fp16 code of value * 2^-8 (subnormals
-                // included); the 2^8 is applied to O at the end
-                uint32_t h16[8];
+                for (int qq = c0; qq < D * 8; qq += 128) {
+                    const int dd = qq >> 3, c = qq & 7;
+                    const uint4 w = *reinterpret_cast<const uint4*>(src + dd * 128 + ((c ^ (dd & 7)) << 4));
+                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                    // e4m3 -> fp16 with integer operations: sign to bit 15, the other 7
+                    // bits to bits 7-13, which is the fp16 code of value * 2^-8
+                    // (subnormals included); the 2^8 is applied to O at the end
+                    uint32_t h16[8];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const uint32_t lo = __byte_perm(ws[e], 0u, 0x1404u);   // [0, b0, 0, b1]
-                    const uint32_t hi = __byte_perm(ws[e], 0u, 0x3424u);   // [0, b2, 0, b3]
-                    h16[2 * e] = (lo & 0x80008000u) | ((lo >> 1) & 0x3F803F80u);
-                    h16[2 * e + 1] = (hi & 0x80008000u) | ((hi >> 1) & 0x3F803F80u);
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t lo = __byte_perm(ws[e], 0u, 0x1404u);   // [0, b0, 0, b1]
+                        const uint32_t hi = __byte_perm(ws[e], 0u, 0x3424u);   // [0, b2, 0, b3]
+                        h16[2 * e] = (lo & 0x80008000u) | ((lo >> 1) & 0x3F803F80u);
+                        h16[2 * e + 1] = (hi & 0x80008000u) | ((hi >> 1) & 0x3F803F80u);
+                    }
+                    uint8_t* dblk = dst + (c >> 2) * (D * 128) + dd * 128;
+                    const int cb = (c & 3) * 2;
+                    *reinterpret_cast<uint4*>(dblk + (((cb + 0) ^ (dd & 7)) << 4)) =
+                        make_uint4(h16[0], h16[1], h16[2], h16[3]);
+                    *reinterpret_cast<uint4*>(dblk + (((cb + 1) ^ (dd & 7)) << 4)) =
+                        make_uint4(h16[4], h16[5], h16[6], h16[7]);
                 }
-                uint8_t* dblk = dst + (c >> 2) * (D * 128) + dd * 128;
-                const int cb = (c & 3) * 2;
-                *reinterpret_cast<uint4*>(dblk + (((cb + 0) ^ (dd & 7)) << 4)) = make_uint4(h16[0], h16[1], h16[2], h16[3]);
-                *reinterpret_cast<uint4*>(dblk + (((cb + 1) ^ (dd & 7)) << 4)) = make_uint4(h16[4], h16[5], h16[6], h16[7]);
+                fence_proxy_async_smem();
+                mbar_arrive(&bars[kBVF + b]);
             }
-            fence_proxy_async_smem();
-            mbar_arrive(&bars[kBVF + b]);
             mbar_arrive(&bars[kBKVE + st]);
         }
     } else if (warp == 12) {
         // ------------------------------------------------------------ TMA producer
+        // The split's tiles twice: K (and the amax rows) for the first pass, then K,
+        // V and the amax rows for the second.
         if (lane == 0) {
             prefetch_tmap(&maps.q8);
             prefetch_tmap(&maps.k8);
@@ -601,65 +644,69 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
             if (nq == 2) tma_load_3d(sQ + L::kQ, &maps.q8, &bars[kBQ], 0, (2 * pair + 1) * 128, h);
             q_issued = true;
         }
-        for (int it = 0; it < nt; ++it) {
-            const int st = it % NST;
-            if (it >= NST && !warp_wait(&bars[kBKVE + st], (uint32_t)(((it / NST) - 1) & 1), sAbort, p, kWaitKVEmpty))
+        for (int ld = 0; ld < 2 * nt; ++ld) {
+            const int st = ld % NST;
+            if (ld >= NST && !warp_wait(&bars[kBKVE + st], (uint32_t)(((ld / NST) - 1) & 1), sAbort, p, kWaitKVEmpty))
                 break;
-            const int j = j0 + it;
+            const int j = j0 + ld % nt;
+            const bool second = ld >= nt;
             if (lane == 0 && j != p.skip_tile) {
-                mbar_expect_tx(&bars[kBKVF + st], (uint32_t)(L::kK + L::kV + L::kAm));
+                mbar_expect_tx(&bars[kBKVF + st], (uint32_t)(L::kK + L::kAmRows + (second ? L::kV : 0)));
                 tma_load_3d(sK + st * L::kK, &maps.k8, &bars[kBKVF + st], 0, j * 128, zrow);
-                tma_load_3d(sV + st * L::kV, &maps.vt8, &bars[kBKVF + st], j * 128, 0, zrow);
+                if (second) tma_load_3d(sV + st * L::kV, &maps.vt8, &bars[kBKVF + st], j * 128, 0, zrow);
                 bulk_g2s(sAm + st * L::kAm, kam + (size_t)j * 128, 512, &bars[kBKVF + st]);
                 bulk_g2s(sAm + st * L::kAm + 512, vam + (size_t)j * 128, 512, &bars[kBKVF + st]);
                 issued[st]++;
             }
             __syncwarp();
         }
-    } else if (warp == 13) {
-        // ------------------------------------------------------------ MMA issuer
-        const uint32_t aQ = smem_u32(sQ);
-        const uint32_t aK = smem_u32(sK);
-        const uint32_t aV16 = smem_u32(sV16);
-        bool ok = warp_wait(&bars[kBQ], 0, sAbort, p, kWaitQ) && warp_wait(&bars[kBKVF], 0, sAbort, p, kWaitKVFull);
-        if (ok) {
-            tc_fence_after();
-            if (lane == 0) {
-                for (int qq = 0; qq < nq; ++qq) {
-                    issue_s<D>(tmem + 128 * qq, aQ + qq * L::kQ, aK);
-                    mma_commit(&bars[kBSF + qq]);
+    } else if (warp == 13 || warp == 14) {
+        // ------------------------------------------------------------ MMA issuers
+        // Warp 13 drives query tile 0, warp 14 query tile 1.  Half u uses S buffer
+        // u % 2.  First pass: S_q(u + 2) as soon as the softmax has read S_q(u) out.
+        // Second pass: O_q += P_q(u) V as soon as P_q(u) is written, then, into the
+        // same buffer, S_q(u + 2); the tensor pipe runs them in that order, so S
+        // never overwrites P before it is read.
+        const int qq = warp - 13;
+        if (qq < nq) {
+            const uint32_t tSq = tmem + 128 * qq;
+            const uint32_t tOq = tmem + 256 + 128 * qq;
+            const uint32_t aQ = smem_u32(sQ) + qq * L::kQ;
+            const uint32_t aK = smem_u32(sK);
+            const uint32_t aV16 = smem_u32(sV16);
+            bool ok = warp_wait(&bars[kBQ], 0, sAbort, p, kWaitQ) && warp_wait(&bars[kBKVF], 0, sAbort, p, kWaitKVFull);
+            if (ok) {
+                tc_fence_after();
+                if (lane == 0) {
+                    issue_s_half<D>(tSq, aQ, aK);
+                    mma_commit(&bars[kBSF + 2 * qq]);
+                    issue_s_half<D>(tSq + 64, aQ, aK + 64 * D);
+                    mma_commit(&bars[kBSF + 2 * qq + 1]);
                 }
-                mma_commit(&bars[kBKVE]);
+                __syncwarp();
             }
-            __syncwarp();
-        }
-        // Per tile j and query tile q: O_q += P_q(j) V_j goes out as soon as P_q(j)
-        // is in tensor memory, followed directly by S_q(j+1) = Q_q K_{j+1}^T, and
-        // one commit covers both (a commit holds the issuing thread until the
-        // tensor pipe has taken the MMAs in, so there are as few as possible).
-        for (int it = 0; ok && it < nt; ++it) {
-            const int stn = (it + 1) % NST, b = it & 1;
-            const bool has_next = it + 1 < nt;
-            if (has_next) {
-                ok = warp_wait(&bars[kBKVF + stn], (uint32_t)(((it + 1) / NST) & 1), sAbort, p, kWaitKVFull);
-                if (!ok) break;
-            }
-            ok = warp_wait(&bars[kBVF + b], (uint32_t)((it >> 1) & 1), sAbort, p, kWaitV16Full);
-            for (int qq = 0; qq < nq && ok; ++qq) {
-                ok = warp_wait(&bars[kBPF + qq], (uint32_t)(it & 1), sAbort, p, kWaitP);
+            for (int u = 0; ok && u < nu; ++u) {
+                const int ld = u >> 1, hb = u & 1;
+                const bool main = u >= nh;
+                const int it = ld - nt;   // second-pass tile of this half
+                if (main && hb == 0) ok = warp_wait(&bars[kBVF + (it & 1)], (uint32_t)((it >> 1) & 1), sAbort, p, kWaitV16Full);
+                ok = ok && warp_wait(&bars[kBPF + 2 * qq + hb], (uint32_t)(ld & 1), sAbort, p, kWaitP);
+                const int ldn = ld + 1, stn = ldn % NST;   // the stage load of half u + 2
+                const bool has_next = u + 2 < nu;
+                if (ok && has_next && hb == 0)
+                    ok = warp_wait(&bars[kBKVF + stn], (uint32_t)((ldn / NST) & 1), sAbort, p, kWaitKVFull);
                 if (!ok) break;
                 tc_fence_after();
                 if (lane == 0) {
-                    issue_pv<D>(tmem + 256 + 128 * qq, tmem + 128 * qq, aV16 + b * L::kV16, it > 0);
-                    if (has_next) {
-                        issue_s<D>(tmem + 128 * qq, aQ + qq * L::kQ, aK + stn * L::kK);
-                        mma_commit(&bars[kBSF + qq]);
-                    } else {
-                        mma_commit(&bars[kBOF + qq]);
+                    if (main) {
+                        issue_pv_half<D>(tOq, tSq + 64 * hb, aV16 + (it & 1) * L::kV16 + hb * (D * 128), u > nh);
+                        if (hb == 1) mma_commit(&bars[kBVE + (it & 1)]);
                     }
-                    if (qq == nq - 1) {
-                        if (has_next) mma_commit(&bars[kBKVE + stn]);
-                        mma_commit(&bars[kBVE + b]);
+                    if (has_next) {
+                        issue_s_half<D>(tSq + 64 * hb, aQ, aK + stn * L::kK + hb * 64 * D);
+                        mma_commit(&bars[kBSF + 2 * qq + hb]);
+                    } else if (u == nu - 1) {
+                        mma_commit(&bars[kBOF + qq]);
                     }
                 }
                 __syncwarp();
@@ -682,8 +729,8 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
     }
     const bool aborted = *sAbort != 0;
     if (aborted) {
-        // nothing of ours may still be in flight when the CTA exits
-        if (warp == 13 && lane == 0) {
+        // nothing of ours may still be in flight when the CTA goes on
+        if ((warp == 13 || warp == 14) && warp - 13 < nq && lane == 0) {
             mma_commit(&bars[kBDrain]);
             mbar_wait(&bars[kBDrain], 0, p.timeout_ns);
         }
@@ -692,86 +739,30 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
             for (int st = 0; st < NST; ++st)
                 if (issued[st] > 0) mbar_wait(&bars[kBKVF + st], (uint32_t)((issued[st] - 1) & 1), p.timeout_ns);
         }
-    } else if (warp < 8 && q < nq) {
-        // ------------------------------------------------------------ epilogue
+        __syncthreads();
+    }
+    // ---------------------------------------------------------------- epilogue
+    // Every stage is consumed (or drained), so the tiles' shared memory is free:
+    // each softmax thread puts its row of O (unnormalised) and its (M, l) there,
+    // and the rows then go out one warp per row (coalesced 512-byte stores):
+    // normalised to out with one KV split, else as this split's partial.
+    constexpr int kORow = D + 4;   // padded row of O in shared memory (fp32)
+    float* sO = reinterpret_cast<float*>(smem);                            // [256][kORow]
+    float2* sML = reinterpret_cast<float2*>(smem + 256 * kORow * 4);       // [256]
+    if (warp < 8 && q < nq) {
         const uint32_t tO = tmem + 256 + 128 * q + ((uint32_t)(wq * 32) << 16);
-        const bool store = qrow < p.T;
-        const bool direct = p.splits == 1;
-        const float f = direct ? 256.f / l_run : 256.f;   // V was widened as V * 2^-8
-        const size_t prow_i = ((size_t)split * p.H + h) * p.Tstride + qrow;
-        float* dst = direct ? p.out + ((size_t)qrow * p.H + h) * D : p.part_o + prow_i * D;
+        float* orow = sO + (size_t)(q * 128 + row) * kORow;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t r[32];
             tmem_ld32(tO + cc * 32, r);
-            if (store) {
 #pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    *reinterpret_cast<float4*>(dst + cc * 32 + e) =
-                        make_float4(__uint_as_float(r[e]) * f, __uint_as_float(r[e + 1]) * f,
-                                    __uint_as_float(r[e + 2]) * f, __uint_as_float(r[e + 3]) * f);
-            }
+            for (int e = 0; e < 32; e += 4)
+                *reinterpret_cast<float4*>(orow + cc * 32 + e) =
+                    make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
+                                __uint_as_float(r[e + 3]));
         }
-        if (store && !direct) *reinterpret_cast<float2*>(p.part_ml + prow_i * 2) = make_float2(M, l_run);
-    }
-    if (p.splits > 1) {
-        // Split merge.  Every CTA counts itself in, aborted or not, so the
-        // per-(head, pair) counter is back at zero after every call; the last
-        // split of the (head, query pair) to arrive merges all partials.
-        __threadfence();
-        __syncthreads();
-        int* counter = p.counters + (size_t)h * (p.Tstride / 256) + pair;
-        if (tid == 0) *sLast = atomicAdd(counter, 1) == p.splits - 1;
-        __syncthreads();
-        if (*sLast) {
-            __threadfence();
-            // each item is 16 output values of one row; all splits' partials for it
-            // are loaded before any is used (at most kMaxSplits of them)
-            const int rows = nq * 128;
-            for (int item = tid; item < rows * (D / 16); item += kAttendThreads) {
-                const int rr = item / (D / 16), c16 = item % (D / 16);
-                const int t = pair * 256 + rr;
-                if (t >= p.T) continue;
-                float2 ml[kMaxSplits];
-                float4 o[kMaxSplits][4];
-#pragma unroll
-                for (int sp = 0; sp < kMaxSplits; ++sp) {
-                    if (sp < p.splits) {
-                        const size_t pr = ((size_t)sp * p.H + h) * p.Tstride + t;
-                        ml[sp] = __ldcg(reinterpret_cast<const float2*>(p.part_ml + pr * 2));
-#pragma unroll
-                        for (int k4 = 0; k4 < 4; ++k4)
-                            o[sp][k4] = __ldcg(reinterpret_cast<const float4*>(p.part_o + pr * D + c16 * 16 + k4 * 4));
-                    }
-                }
-                float M = -INFINITY;
-#pragma unroll
-                for (int sp = 0; sp < kMaxSplits; ++sp)
-                    if (sp < p.splits) M = fmaxf(M, ml[sp].x);
-                float lsum = 0.f;
-                float4 acc[4];
-#pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) acc[k4] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int sp = 0; sp < kMaxSplits; ++sp) {
-                    if (sp < p.splits) {
-                        const float w = ex2_approx(ml[sp].x - M);
-                        lsum += w * ml[sp].y;
-#pragma unroll
-                        for (int k4 = 0; k4 < 4; ++k4) {
-                            acc[k4].x += w * o[sp][k4].x; acc[k4].y += w * o[sp][k4].y;
-                            acc[k4].z += w * o[sp][k4].z; acc[k4].w += w * o[sp][k4].w;
-                        }
-                    }
-                }
-                const float inv = 1.f / lsum;
-                float4* dst = reinterpret_cast<float4*>(p.out + ((size_t)t * p.H + h) * D + c16 * 16);
-#pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4)
-                    dst[k4] = make_float4(acc[k4].x * inv, acc[k4].y * inv, acc[k4].z * inv, acc[k4].w * inv);
-            }
-            if (tid == 0) *counter = 0;
-        }
+        sML[q * 128 + row] = make_float2(M, l_run);
     }
     tc_fence_before();
     __syncthreads();
@@ -779,10 +770,84 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
-}
-
-size_t attend_smem_bytes(int d) {
-    return d == 128 ? (size_t)AttendSmem<128>::kAlloc : (size_t)AttendSmem<64>::kAlloc;
+    const int rows = nq * 128;
+    const bool lanes_d = lane < D / 4;   // lane i holds output values 4i..4i+3
+    if (p.splits == 1) {
+        for (int rr = warp; rr < rows; rr += kAttendThreads / 32) {
+            const int t = pair * 256 + rr;
+            if (t >= p.T || !lanes_d) continue;
+            const float f = 256.f / sML[rr].y;   // V was widened as V * 2^-8
+            const float4 o = *reinterpret_cast<const float4*>(sO + (size_t)rr * kORow + 4 * lane);
+            *reinterpret_cast<float4*>(p.out + ((size_t)t * p.H + h) * D + 4 * lane) =
+                make_float4(o.x * f, o.y * f, o.z * f, o.w * f);
+        }
+        return;
+    }
+    // partial of this split: O * 2^8 (unnormalised) and (M, l) per row
+    for (int rr = warp; rr < rows; rr += kAttendThreads / 32) {
+        const int t = pair * 256 + rr;
+        if (t >= p.T) continue;
+        const size_t pr = ((size_t)split * p.H + h) * p.Tstride + t;
+        if (lanes_d) {
+            const float4 o = *reinterpret_cast<const float4*>(sO + (size_t)rr * kORow + 4 * lane);
+            *reinterpret_cast<float4*>(p.part_o + pr * D + 4 * lane) =
+                make_float4(o.x * 256.f, o.y * 256.f, o.z * 256.f, o.w * 256.f);
+        }
+        if (lane == 0) *reinterpret_cast<float2*>(p.part_ml + pr * 2) = sML[rr];
+    }
+    // Split merge.  Every CTA counts itself in, aborted or not, so the per-(head,
+    // pair) counter is back at zero after every call; the last split of the
+    // (head, query pair) to arrive merges all partials, one warp per row, four
+    // rows per warp at a time with all their loads in flight.
+    __threadfence();
+    __syncthreads();
+    int* counter = p.counters + (size_t)h * (p.Tstride / 256) + pair;
+    if (tid == 0) *sLast = atomicAdd(counter, 1) == p.splits - 1;
+    __syncthreads();
+    if (!*sLast) return;
+    __threadfence();
+    constexpr int kRowsAtOnce = 4;
+    for (int rb = warp * kRowsAtOnce; rb < rows; rb += kRowsAtOnce * (kAttendThreads / 32)) {
+        float2 ml[kRowsAtOnce][kMaxSplits];
+        float4 o[kRowsAtOnce][kMaxSplits];
+#pragma unroll
+        for (int k = 0; k < kRowsAtOnce; ++k) {
+            const int t = pair * 256 + rb + k;
+#pragma unroll
+            for (int sp = 0; sp < kMaxSplits; ++sp) {
+                ml[k][sp] = make_float2(-INFINITY, 0.f);
+                o[k][sp] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (sp < p.splits && t < p.T) {
+                    const size_t pr = ((size_t)sp * p.H + h) * p.Tstride + t;
+                    ml[k][sp] = __ldcg(reinterpret_cast<const float2*>(p.part_ml + pr * 2));
+                    if (lanes_d) o[k][sp] = __ldcg(reinterpret_cast<const float4*>(p.part_o + pr * D + 4 * lane));
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kRowsAtOnce; ++k) {
+            const int t = pair * 256 + rb + k;
+            if (t >= p.T || !lanes_d) continue;
+            float mx = ml[k][0].x;
+#pragma unroll
+            for (int sp = 1; sp < kMaxSplits; ++sp) mx = fmaxf(mx, ml[k][sp].x);
+            float lw = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int sp = 0; sp < kMaxSplits; ++sp) {
+                const float w = sp < p.splits ? ex2_approx(ml[k][sp].x - mx) : 0.f;
+                lw = fmaf(w, ml[k][sp].y, lw);
+                acc.x = fmaf(w, o[k][sp].x, acc.x);
+                acc.y = fmaf(w, o[k][sp].y, acc.y);
+                acc.z = fmaf(w, o[k][sp].z, acc.z);
+                acc.w = fmaf(w, o[k][sp].w, acc.w);
+            }
+            const float inv = 1.f / lw;
+            *reinterpret_cast<float4*>(p.out + ((size_t)t * p.H + h) * D + 4 * lane) =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        }
+    }
+    if (tid == 0) *counter = 0;
 }
 
 cudaError_t launch_attend(const AttendParams& p, const AttendMaps& maps, cudaStream_t s) {
