@@ -39,6 +39,9 @@ namespace kvring_impl {
 // e4m3 with its own amax, write [H][Tstride][d] codes + [H][Tstride] amax.
 // Rows T..Tpad-1 are written as zeros.
 __global__ void __launch_bounds__(128) qprep_kernel(const __grid_constant__ QPrepParams p) {
+    // the attention kernel that follows may start its own set-up (it waits for
+    // this grid before it touches Q)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int d = p.d;
     const int tpr = d / 8;                       // threads per row, 8 elements each
     const int rows_per_block = 128 / tpr;
@@ -121,7 +124,7 @@ struct AttendSmem {
     static constexpr int kAm = kAmRows + 4 * 32;
     static constexpr int offAm = offV16 + 2 * kV16;
     static constexpr int offBar = offAm + kStages * kAm;
-    static constexpr int kBars = 25;
+    static constexpr int kBars = 33;
     static constexpr int offMisc = offBar + kBars * 8;
     static constexpr int kBytes = offMisc + 64;
     static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
@@ -139,6 +142,8 @@ enum : int {
     kBOF = 19,      // [2] O_q complete: the last O_q += P V (commit)
     kBDrain = 21,   // drain after an abort (one commit per active issuer)
     kBIF = 22,      // [3] the stage's group summaries written (one arrival per converter warp)
+    kBSF1 = 25,     // [2][2] first pass: S_q of a full tile in buffer b computed (commit)
+    kBPF1 = 29,     // [2][2] first pass: that S read out (one arrival per softmax warp)
 };
 enum : int { kWaitQ = 1, kWaitKVFull = 2, kWaitKVEmpty = 3, kWaitS = 4, kWaitP = 5, kWaitO = 6, kWaitV16Full = 7,
              kWaitV16Empty = 8 };
@@ -156,10 +161,11 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
                                           const AttendParams& p, int site) {
     int ok = 1;
     if ((threadIdx.x & 31) == 0) {
-        if (!mbar_test_wait(bar, parity) && !mbar_try_wait(bar, parity)) {
+        if (!mbar_test_wait(bar, parity)) {
+            // spin on test_wait: a suspended try_wait wakes up measurably later
             const uint64_t t0 = globaltimer_ns();
             while (true) {
-                if (mbar_try_wait(bar, parity)) break;
+                if (mbar_test_wait(bar, parity)) break;
                 if (*abort_flag) { ok = 0; break; }
                 if ((long long)(globaltimer_ns() - t0) > p.timeout_ns) {
                     *abort_flag = 1;
@@ -175,6 +181,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
         }
     }
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// S for one full tile: S[128 query rows][128 slots] = Q K^T (first pass).
+template <int D>
+__device__ __forceinline__ void issue_s_full(uint32_t tS, uint32_t aQ, uint32_t aK) {
+    constexpr uint32_t id = make_idesc(128, 128);
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k)
+        mma_f8(tS, make_sdesc(aQ + k * 32, D), make_sdesc(aK + k * 32, D), id, k > 0 ? 1u : 0u);
 }
 
 // S for one half tile: S[128 query rows][64 slots] = Q K_half^T, e4m3 operands in
@@ -437,8 +452,8 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
         // widened) and one arrival per softmax warp of each active query tile (at
         // the end of its tile: its S MMAs are done and its scale rows read).
         const int kve = 128 + 4 * nq;
-        const int counts[L::kBars] = {1, 1, 1, 1, kve, kve, kve, 1,  1,  1,  1, 4, 4,
-                                      4, 4, 128, 128, nq, nq, 1,  1,  nq, 4, 4, 4};
+        const int counts[L::kBars] = {1, 1, 1, 1, kve, kve, kve, 1,  1,  1,  1, 4, 4, 4, 4, 128, 128,
+                                      nq, nq, 1,  1,  nq, 4, 4, 4, 1, 1, 1, 1,  4, 4, 4, 4};
         for (int b = 0; b < L::kBars; ++b) mbar_init(&bars[b], counts[b]);
         fence_mbar_init();
         *sAbort = 0;
@@ -449,7 +464,6 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
     tc_fence_after();
     const uint32_t tmem = *sTmem;
     const int nh = 2 * nt;   // half tiles of 64 slots in one pass over the split
-    const int nu = 2 * nh;   // both passes
 
     // softmax state (warps 0-7), kept for the epilogue
     const int q = warp >> 2;
@@ -482,46 +496,94 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
         // row sum takes it out again with 1/sv.
         // Two passes over the split's slots: the first computes S only and keeps the
         // exact row max M of z; the second computes P = 2^(z - M) <= 1 and O += P V
-        // with M fixed, so O is never rescaled.  Each 128-slot tile is worked in two
-        // halves of 64, each with its own S buffer in tensor memory, so that S of the
-        // next half is computed while this one is worked on.
+        // with M fixed, so O is never rescaled.  Either pass has two S buffers per
+        // query tile, so that the next S is computed while this one is worked on:
+        // the first pass uses full tiles in S_q and (while it is unused) O_q, the
+        // second half tiles of 64 slots in the two halves of S_q.
         const bool active = q < nq;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t tS = tmem + 128 * q + lane_off;
+        const uint32_t tO = tmem + 256 + 128 * q + lane_off;
+        asm volatile("griddepcontrol.wait;" ::: "memory");   // Q prep has finished
         const float a = scale_of(__ldg(p.qamax + (size_t)h * p.Tstride + qrow)) * p.log2e_rsqrt_d;
         float gk[4], gl[4], gi[4];
         bool uni[2];
         const float* am = nullptr;
         const GroupInfo* info = nullptr;
         int slot0 = 0;
-        for (int u = 0; active && u < nu; ++u) {
-            const int ld = u >> 1, hb = u & 1, st = ld % NST;   // ld: the stage load this half reads
-            const bool main = u >= nh;
-            const uint32_t tSb = tS + 64 * hb;
-            if (hb == 0) {
-                slot0 = (j0 + ld % nt) * 128;
-                am = reinterpret_cast<const float*>(sAm + st * L::kAm);   // K amax [128], V amax [128]
-                info = reinterpret_cast<const GroupInfo*>(sAm + st * L::kAm + L::kAmRows);
-                // Tile setup from the converter's group summaries.  The columns of one
-                // chunk share one pair of scales, so a 32-column group is usually one
-                // range; a half whose two groups both are (the common case) takes the
-                // fast path below.
-                if (!warp_wait(&bars[kBIF + st], (uint32_t)((ld / NST) & 1), sAbort, p, kWaitKVFull)) break;
-                int kinds = 0;
+        // Tile setup from the converter's group summaries of stage load ld.  The
+        // columns of one chunk share one pair of scales, so a 32-column group is
+        // usually one range; a half whose two groups both are (the common case)
+        // takes the fast path below.
+        auto tile_setup = [&](int ld) -> bool {
+            const int st = ld % NST;
+            slot0 = (j0 + ld % nt) * 128;
+            am = reinterpret_cast<const float*>(sAm + st * L::kAm);   // K amax [128], V amax [128]
+            info = reinterpret_cast<const GroupInfo*>(sAm + st * L::kAm + L::kAmRows);
+            if (!warp_wait(&bars[kBIF + st], (uint32_t)((ld / NST) & 1), sAbort, p, kWaitKVFull)) return false;
+            int kinds = 0;
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const float4 i0 = reinterpret_cast<const float4*>(info + g)[0];
-                    gk[g] = i0.x * a;   // a is this thread's own row's
-                    gl[g] = i0.y;
-                    gi[g] = i0.z;
-                    kinds |= (__float_as_int(i0.w) & 3) << (8 * g);
-                }
-                uni[0] = (kinds & 0xFFFF) == 0;
-                uni[1] = (kinds >> 16) == 0;
+            for (int g = 0; g < 4; ++g) {
+                const float4 i0 = reinterpret_cast<const float4*>(info + g)[0];
+                gk[g] = i0.x * a;   // a is this thread's own row's
+                gl[g] = i0.y;
+                gi[g] = i0.z;
+                kinds |= (__float_as_int(i0.w) & 3) << (8 * g);
             }
-            const bool un = hb == 0 ? uni[0] : uni[1];
+            uni[0] = (kinds & 0xFFFF) == 0;
+            uni[1] = (kinds >> 16) == 0;
+            return true;
+        };
+        // row max of z over two groups (g0, g0 + 1) held in registers
+        auto zmax2 = [&](const uint32_t (&ra)[32], const uint32_t (&rb)[32], int hb) -> float {
+            if (uni[hb])
+                return fmaxf(fmaf(max32(ra), hb ? gk[2] : gk[0], hb ? gl[2] : gl[0]),
+                             fmaf(max32(rb), hb ? gk[3] : gk[1], hb ? gl[3] : gl[1]));
+            return fmaxf(zmax_group(ra, group_scales(info, am, 2 * hb, slot0, p.count, a, lane), a),
+                         zmax_group(rb, group_scales(info, am, 2 * hb + 1, slot0, p.count, a, lane), a));
+        };
+        // First pass, one full tile at a time in S buffer j % 2 (S_q or, while it is
+        // unused, O_q's columns): the row max M of z.
+        for (int j = 0; active && j < nt; ++j) {
+            const int st = j % NST, b = j & 1;
+            if (!tile_setup(j)) break;
+            if (!warp_wait(&bars[kBSF1 + 2 * q + b], (uint32_t)((j >> 1) & 1), sAbort, p, kWaitS)) break;
+            tc_fence_after();
+            const uint32_t tSj = b ? tO : tS;
+            float tz;
+            {
+                uint32_t ra[32], rb[32];
+                tmem_ld32_async(tSj, ra);
+                tmem_ld32_async(tSj + 32, rb);
+                tmem_wait_ld_dep(ra);
+                tmem_dep(rb);
+                tz = zmax2(ra, rb, 0);
+            }
+            {
+                uint32_t ra[32], rb[32];
+                tmem_ld32_async(tSj + 64, ra);
+                tmem_ld32_async(tSj + 96, rb);
+                tmem_wait_ld_dep(ra);
+                tmem_dep(rb);
+                // the buffer is free again once read
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kBPF1 + 2 * q + b]);
+                tz = fmaxf(tz, zmax2(ra, rb, 1));
+            }
+            M = fmaxf(M, tz);
+            // the end of the stage: its S MMAs are done and its scale rows read
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kBKVE + st]);
+        }
+        // Second pass, half tiles: P = 2^(z - M) <= 1 with M fixed.
+        for (int u = 0; active && u < nh; ++u) {
+            const int ld = nt + (u >> 1), hb = u & 1, st = ld % NST;   // ld: the stage load this half reads
+            const uint32_t tSb = tS + 64 * hb;
+            if (hb == 0 && !tile_setup(ld)) break;
+            const bool un = uni[hb];
             const int g0 = 2 * hb;   // the half's groups are g0 and g0 + 1
-            if (!warp_wait(&bars[kBSF + 2 * q + hb], (uint32_t)(ld & 1), sAbort, p, kWaitS)) break;
+            if (!warp_wait(&bars[kBSF + 2 * q + hb], (uint32_t)((u >> 1) & 1), sAbort, p, kWaitS)) break;
             tc_fence_after();
             // the half's S (two groups of 32 columns), read once into registers
             uint32_t ra[32], rb[32];
@@ -529,27 +591,13 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
             tmem_ld32_async(tSb + 32, rb);
             tmem_wait_ld_dep(ra);
             tmem_dep(rb);
-            if (!main) {
-                // first pass: row max of z; the S buffer is free again once read
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[kBPF + 2 * q + hb]);
-                float tz;
-                if (un) {
-                    tz = fmaxf(fmaf(max32(ra), hb ? gk[2] : gk[0], hb ? gl[2] : gl[0]),
-                               fmaf(max32(rb), hb ? gk[3] : gk[1], hb ? gl[3] : gl[1]));
-                } else {
-                    tz = fmaxf(zmax_group(ra, group_scales(info, am, g0, slot0, p.count, a, lane), a),
-                               zmax_group(rb, group_scales(info, am, g0 + 1, slot0, p.count, a, lane), a));
-                }
-                M = fmaxf(M, tz);
-            } else {
-                // second pass: P = 2^(z - M) as fp16, written over the half's S buffer
-                // (group g of the half to columns [16g, 16g + 16), which hold only
-                // values already read).  The row sum must use the same (rounded)
-                // weights that O += P V sees wherever one weight dominates: a one-range
-                // group sums the fp32 P and adds back the fp16 rounding of its largest
-                // element (the row's dominant weight is always one of them; the other
+            {
+                // P = 2^(z - M) as fp16, written over the half's S buffer (group g of
+                // the half to columns [16g, 16g + 16), which hold only values already
+                // read).  The row sum must use the same (rounded) weights that
+                // O += P V sees wherever one weight dominates: a one-range group sums
+                // the fp32 P and adds back the fp16 rounding of its largest element
+                // (the row's dominant weight is always one of them; the other
                 // elements' rounding is at most 2^-12 of their own, non-dominant,
                 // share); the other kinds sum the rounded values.
                 uint32_t pk[16];
@@ -639,12 +687,17 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
             prefetch_tmap(&maps.q8);
             prefetch_tmap(&maps.k8);
             prefetch_tmap(&maps.vt8);
-            mbar_expect_tx(&bars[kBQ], (uint32_t)(nq * L::kQ));
-            tma_load_3d(sQ, &maps.q8, &bars[kBQ], 0, (2 * pair) * 128, h);
-            if (nq == 2) tma_load_3d(sQ + L::kQ, &maps.q8, &bars[kBQ], 0, (2 * pair + 1) * 128, h);
-            q_issued = true;
         }
         for (int ld = 0; ld < 2 * nt; ++ld) {
+            if (ld == (nt < NST ? nt : NST) && lane == 0) {
+                // the query tiles, once the first stages are on their way and Q prep
+                // (the grid before this one) has finished
+                asm volatile("griddepcontrol.wait;" ::: "memory");
+                mbar_expect_tx(&bars[kBQ], (uint32_t)(nq * L::kQ));
+                tma_load_3d(sQ, &maps.q8, &bars[kBQ], 0, (2 * pair) * 128, h);
+                if (nq == 2) tma_load_3d(sQ + L::kQ, &maps.q8, &bars[kBQ], 0, (2 * pair + 1) * 128, h);
+                q_issued = true;
+            }
             const int st = ld % NST;
             if (ld >= NST && !warp_wait(&bars[kBKVE + st], (uint32_t)(((ld / NST) - 1) & 1), sAbort, p, kWaitKVEmpty))
                 break;
@@ -674,38 +727,57 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
             const uint32_t aQ = smem_u32(sQ) + qq * L::kQ;
             const uint32_t aK = smem_u32(sK);
             const uint32_t aV16 = smem_u32(sV16);
-            bool ok = warp_wait(&bars[kBQ], 0, sAbort, p, kWaitQ) && warp_wait(&bars[kBKVF], 0, sAbort, p, kWaitKVFull);
-            if (ok) {
+            bool ok = warp_wait(&bars[kBQ], 0, sAbort, p, kWaitQ);
+            // First pass: full tiles j in buffer j % 2 (S_q, O_q); S(j + 2) as soon as
+            // the softmax has read S(j) out.
+            for (int j = 0; ok && j < nt + 2; ++j) {
+                if (j >= 2) {
+                    ok = warp_wait(&bars[kBPF1 + 2 * qq + (j & 1)], (uint32_t)(((j - 2) >> 1) & 1), sAbort, p, kWaitP);
+                    if (!ok) break;
+                }
+                if (j >= nt) continue;
+                const int st = j % NST;
+                ok = warp_wait(&bars[kBKVF + st], (uint32_t)((j / NST) & 1), sAbort, p, kWaitKVFull);
+                if (!ok) break;
                 tc_fence_after();
                 if (lane == 0) {
-                    issue_s_half<D>(tSq, aQ, aK);
-                    mma_commit(&bars[kBSF + 2 * qq]);
-                    issue_s_half<D>(tSq + 64, aQ, aK + 64 * D);
-                    mma_commit(&bars[kBSF + 2 * qq + 1]);
+                    issue_s_full<D>((j & 1) ? tOq : tSq, aQ, aK + st * L::kK);
+                    mma_commit(&bars[kBSF1 + 2 * qq + (j & 1)]);
                 }
                 __syncwarp();
             }
-            for (int u = 0; ok && u < nu; ++u) {
-                const int ld = u >> 1, hb = u & 1;
-                const bool main = u >= nh;
-                const int it = ld - nt;   // second-pass tile of this half
-                if (main && hb == 0) ok = warp_wait(&bars[kBVF + (it & 1)], (uint32_t)((it >> 1) & 1), sAbort, p, kWaitV16Full);
-                ok = ok && warp_wait(&bars[kBPF + 2 * qq + hb], (uint32_t)(ld & 1), sAbort, p, kWaitP);
-                const int ldn = ld + 1, stn = ldn % NST;   // the stage load of half u + 2
-                const bool has_next = u + 2 < nu;
+            // Second pass: half tiles u in buffer u % 2 of S_q.
+            if (ok) {
+                const int st = nt % NST;
+                ok = warp_wait(&bars[kBKVF + st], (uint32_t)((nt / NST) & 1), sAbort, p, kWaitKVFull);
+                if (ok) {
+                    tc_fence_after();
+                    if (lane == 0) {
+                        issue_s_half<D>(tSq, aQ, aK + st * L::kK);
+                        mma_commit(&bars[kBSF + 2 * qq]);
+                        issue_s_half<D>(tSq + 64, aQ, aK + st * L::kK + 64 * D);
+                        mma_commit(&bars[kBSF + 2 * qq + 1]);
+                    }
+                    __syncwarp();
+                }
+            }
+            for (int u = 0; ok && u < nh; ++u) {
+                const int it = u >> 1, hb = u & 1;   // second-pass tile of this half
+                if (hb == 0) ok = warp_wait(&bars[kBVF + (it & 1)], (uint32_t)((it >> 1) & 1), sAbort, p, kWaitV16Full);
+                ok = ok && warp_wait(&bars[kBPF + 2 * qq + hb], (uint32_t)(it & 1), sAbort, p, kWaitP);
+                const int ldn = nt + it + 1, stn = ldn % NST;   // the stage load of half u + 2
+                const bool has_next = u + 2 < nh;
                 if (ok && has_next && hb == 0)
                     ok = warp_wait(&bars[kBKVF + stn], (uint32_t)((ldn / NST) & 1), sAbort, p, kWaitKVFull);
                 if (!ok) break;
                 tc_fence_after();
                 if (lane == 0) {
-                    if (main) {
-                        issue_pv_half<D>(tOq, tSq + 64 * hb, aV16 + (it & 1) * L::kV16 + hb * (D * 128), u > nh);
-                        if (hb == 1) mma_commit(&bars[kBVE + (it & 1)]);
-                    }
+                    issue_pv_half<D>(tOq, tSq + 64 * hb, aV16 + (it & 1) * L::kV16 + hb * (D * 128), u > 0);
+                    if (hb == 1) mma_commit(&bars[kBVE + (it & 1)]);
                     if (has_next) {
                         issue_s_half<D>(tSq + 64 * hb, aQ, aK + stn * L::kK + hb * 64 * D);
                         mma_commit(&bars[kBSF + 2 * qq + hb]);
-                    } else if (u == nu - 1) {
+                    } else if (u == nh - 1) {
                         mma_commit(&bars[kBOF + qq]);
                     }
                 }
@@ -850,20 +922,26 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
     if (tid == 0) *counter = 0;
 }
 
+// Launched with programmatic stream serialisation: its CTAs may start while the
+// Q prep grid before it is still running; they wait for it (griddepcontrol.wait)
+// before reading Q.
 cudaError_t launch_attend(const AttendParams& p, const AttendMaps& maps, cudaStream_t s) {
     const int grid = p.H * p.npairs * p.splits;
-    if (p.d == 128) {
-        const int smem = AttendSmem<128>::kAlloc;
-        cudaError_t e = cudaFuncSetAttribute(attend_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attend_kernel<128><<<grid, kAttendThreads, smem, s>>>(p, maps);
-    } else {
-        const int smem = AttendSmem<64>::kAlloc;
-        cudaError_t e = cudaFuncSetAttribute(attend_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attend_kernel<64><<<grid, kAttendThreads, smem, s>>>(p, maps);
-    }
-    return cudaGetLastError();
+    const int smem = p.d == 128 ? (int)AttendSmem<128>::kAlloc : (int)AttendSmem<64>::kAlloc;
+    void (*kern)(AttendParams, AttendMaps) = p.d == 128 ? attend_kernel<128> : attend_kernel<64>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kAttendThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p, maps);
 }
 
 }  // namespace kvring_impl
