@@ -189,7 +189,7 @@ __device__ __forceinline__ void issue_s_full(uint32_t tS, uint32_t aQ, uint32_t 
     constexpr uint32_t id = make_idesc(128, 128);
 #pragma unroll
     for (int k = 0; k < D / 32; ++k)
-        mma_f8(tS, make_sdesc(aQ + k * 32, D), make_sdesc(aK + k * 32, D), id, k > 0 ? 1u : 0u);
+        mma_f8_warp(tS, make_sdesc(aQ + k * 32, D), make_sdesc(aK + k * 32, D), id, k > 0 ? 1u : 0u);
 }
 
 // S for one half tile: S[128 query rows][64 slots] = Q K_half^T, e4m3 operands in
@@ -199,7 +199,7 @@ __device__ __forceinline__ void issue_s_half(uint32_t tS, uint32_t aQ, uint32_t 
     constexpr uint32_t id = make_idesc(128, 64);
 #pragma unroll
     for (int k = 0; k < D / 32; ++k)
-        mma_f8(tS, make_sdesc(aQ + k * 32, D), make_sdesc(aK + k * 32, D), id, k > 0 ? 1u : 0u);
+        mma_f8_warp(tS, make_sdesc(aQ + k * 32, D), make_sdesc(aK + k * 32, D), id, k > 0 ? 1u : 0u);
 }
 
 // O += P V for one half tile (64 slots): P (fp16) in tensor memory at tP, 8 columns
@@ -209,7 +209,7 @@ __device__ __forceinline__ void issue_pv_half(uint32_t tO, uint32_t tP, uint32_t
     constexpr uint32_t id = make_idesc(128, D);
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-        mma_f16_ts(tO, tP + k * 8, make_sdesc(aV16blk + k * 32, 128), id, (accumulate || k > 0) ? 1u : 0u);
+        mma_f16_ts_warp(tO, tP + k * 8, make_sdesc(aV16blk + k * 32, 128), id, (accumulate || k > 0) ? 1u : 0u);
 }
 
 __device__ __forceinline__ float lg2_approx(float x) {
@@ -740,11 +740,8 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                 ok = warp_wait(&bars[kBKVF + st], (uint32_t)((j / NST) & 1), sAbort, p, kWaitKVFull);
                 if (!ok) break;
                 tc_fence_after();
-                if (lane == 0) {
-                    issue_s_full<D>((j & 1) ? tOq : tSq, aQ, aK + st * L::kK);
-                    mma_commit(&bars[kBSF1 + 2 * qq + (j & 1)]);
-                }
-                __syncwarp();
+                issue_s_full<D>((j & 1) ? tOq : tSq, aQ, aK + st * L::kK);
+                mma_commit_warp(&bars[kBSF1 + 2 * qq + (j & 1)]);
             }
             // Second pass: half tiles u in buffer u % 2 of S_q.
             if (ok) {
@@ -752,13 +749,10 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                 ok = warp_wait(&bars[kBKVF + st], (uint32_t)((nt / NST) & 1), sAbort, p, kWaitKVFull);
                 if (ok) {
                     tc_fence_after();
-                    if (lane == 0) {
-                        issue_s_half<D>(tSq, aQ, aK + st * L::kK);
-                        mma_commit(&bars[kBSF + 2 * qq]);
-                        issue_s_half<D>(tSq + 64, aQ, aK + st * L::kK + 64 * D);
-                        mma_commit(&bars[kBSF + 2 * qq + 1]);
-                    }
-                    __syncwarp();
+                    issue_s_half<D>(tSq, aQ, aK + st * L::kK);
+                    mma_commit_warp(&bars[kBSF + 2 * qq]);
+                    issue_s_half<D>(tSq + 64, aQ, aK + st * L::kK + 64 * D);
+                    mma_commit_warp(&bars[kBSF + 2 * qq + 1]);
                 }
             }
             for (int u = 0; ok && u < nh; ++u) {
@@ -771,17 +765,15 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                     ok = warp_wait(&bars[kBKVF + stn], (uint32_t)((ldn / NST) & 1), sAbort, p, kWaitKVFull);
                 if (!ok) break;
                 tc_fence_after();
-                if (lane == 0) {
-                    issue_pv_half<D>(tOq, tSq + 64 * hb, aV16 + (it & 1) * L::kV16 + hb * (D * 128), u > 0);
-                    if (hb == 1) mma_commit(&bars[kBVE + (it & 1)]);
-                    if (has_next) {
-                        issue_s_half<D>(tSq + 64 * hb, aQ, aK + stn * L::kK + hb * 64 * D);
-                        mma_commit(&bars[kBSF + 2 * qq + hb]);
-                    } else if (u == nh - 1) {
-                        mma_commit(&bars[kBOF + qq]);
-                    }
+                // the whole warp issues (warp-uniform operands, one elected lane)
+                issue_pv_half<D>(tOq, tSq + 64 * hb, aV16 + (it & 1) * L::kV16 + hb * (D * 128), u > 0);
+                if (hb == 1) mma_commit_warp(&bars[kBVE + (it & 1)]);
+                if (has_next) {
+                    issue_s_half<D>(tSq + 64 * hb, aQ, aK + stn * L::kK + hb * 64 * D);
+                    mma_commit_warp(&bars[kBSF + 2 * qq + hb]);
+                } else if (u == nh - 1) {
+                    mma_commit_warp(&bars[kBOF + qq]);
                 }
-                __syncwarp();
             }
         }
     }
@@ -802,9 +794,10 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
     const bool aborted = *sAbort != 0;
     if (aborted) {
         // nothing of ours may still be in flight when the CTA goes on
-        if ((warp == 13 || warp == 14) && warp - 13 < nq && lane == 0) {
-            mma_commit(&bars[kBDrain]);
-            mbar_wait(&bars[kBDrain], 0, p.timeout_ns);
+        if ((warp == 13 || warp == 14) && warp - 13 < nq) {
+            mma_commit_warp(&bars[kBDrain]);
+            if (lane == 0) mbar_wait(&bars[kBDrain], 0, p.timeout_ns);
+            __syncwarp();
         }
         if (warp == 12 && lane == 0) {
             if (q_issued) mbar_wait(&bars[kBQ], 0, p.timeout_ns);
