@@ -154,36 +154,43 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// Warp-collective bounded wait: lane 0 polls, the verdict is broadcast.  Gives
-// up when the phase does not complete within timeout_ns (and then records the
-// time-out and raises the CTA's abort flag) or when the abort flag is raised.
+// Warp-collective bounded wait: every lane polls the same barrier word with
+// the same instruction, so all see the same state and the warp never diverges
+// (a divergent single-lane poll plus a broadcast costs several hundred cycles
+// even when the phase is already complete).  Gives up when the phase does not
+// complete within timeout_ns (and then records the time-out and raises the
+// CTA's abort flag) or when the abort flag is raised.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           const AttendParams& p, int site) {
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) {
-        if (!mbar_test_wait(bar, parity)) {
-            // spin on test_wait: a suspended try_wait wakes up measurably later
-            const uint64_t t0 = globaltimer_ns();
-            while (true) {
-                if (mbar_test_wait(bar, parity)) break;
-                if (*abort_flag) { ok = 0; break; }
-                if ((long long)(globaltimer_ns() - t0) > p.timeout_ns) {
-                    *abort_flag = 1;
-                    if (atomicCAS(p.err, 0, KVRING_ETIMEOUT) == 0) {
-                        p.err[1] = kKernelAttend;
-                        p.err[2] = site;
-                        p.err[3] = (int)blockIdx.x;
-                    }
-                    ok = 0;
-                    break;
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
+        if (__any_sync(0xffffffffu, (long long)(globaltimer_ns() - t0) > p.timeout_ns)) {
+            if ((threadIdx.x & 31) == 0) {
+                *abort_flag = 1;
+                if (atomicCAS(p.err, 0, KVRING_ETIMEOUT) == 0) {
+                    p.err[1] = kKernelAttend;
+                    p.err[2] = site;
+                    p.err[3] = (int)blockIdx.x;
                 }
             }
+            __syncwarp();
+            return false;
         }
     }
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// S for one full tile: S[128 query rows][128 slots] = Q K^T (first pass).
+// One arrival for the whole warp (elected lane; the warp must be converged).
+__device__ __forceinline__ void mbar_arrive_warp(uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
+}
+
 template <int D>
 __device__ __forceinline__ void issue_s_full(uint32_t tS, uint32_t aQ, uint32_t aK) {
     constexpr uint32_t id = make_idesc(128, 128);
@@ -568,13 +575,13 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                 // the buffer is free again once read
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[kBPF1 + 2 * q + b]);
+                mbar_arrive_warp(&bars[kBPF1 + 2 * q + b]);
                 tz = fmaxf(tz, zmax2(ra, rb, 1));
             }
             M = fmaxf(M, tz);
             // the end of the stage: its S MMAs are done and its scale rows read
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kBKVE + st]);
+            mbar_arrive_warp(&bars[kBKVE + st]);
         }
         // Second pass, half tiles: P = 2^(z - M) <= 1 with M fixed.
         for (int u = 0; active && u < nh; ++u) {
@@ -619,12 +626,12 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[kBPF + 2 * q + hb]);
+                mbar_arrive_warp(&bars[kBPF + 2 * q + hb]);
             }
             if (hb == 1) {
                 // the end of the stage: its S MMAs are done and its scale rows read
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[kBKVE + st]);
+                mbar_arrive_warp(&bars[kBKVE + st]);
             }
         }
         if (active && !*sAbort) {
@@ -644,7 +651,7 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
             write_group_info(reinterpret_cast<const float*>(sAm + st * L::kAm), warp - 8, (j0 + ld % nt) * 128, p.count,
                              lane, reinterpret_cast<GroupInfo*>(sAm + st * L::kAm + L::kAmRows) + (warp - 8));
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kBIF + st]);
+            mbar_arrive_warp(&bars[kBIF + st]);
             if (ld >= nt) {
                 const int it = ld - nt, b = it & 1;
                 if (it >= 2 && !warp_wait(&bars[kBVE + b], (uint32_t)(((it >> 1) - 1) & 1), sAbort, p, kWaitV16Empty))
