@@ -134,10 +134,10 @@ struct AttendSmem {
 enum : int {
     kBQ = 0,        // query tiles landed (TMA)
     kBKVF = 1,      // [3] stage full: K, V and the amax rows (TMA)
-    kBKVE = 4,      // [3] stage free: 128 converter arrivals + one per softmax warp (end of its tile)
+    kBKVE = 4,      // [3] stage free: one arrival per converter warp and per softmax warp (end of its tile)
     kBSF = 7,       // [2][2] S_q half b computed (commit)
     kBPF = 11,      // [2][2] first pass: S_q half b read out; second: P_q half b written (one arrival per softmax warp)
-    kBVF = 15,      // [2] fp16 V buffer full (128 converter arrivals)
+    kBVF = 15,      // [2] fp16 V buffer full (one arrival per converter warp)
     kBVE = 17,      // [2] fp16 V buffer free (one commit per active issuer)
     kBOF = 19,      // [2] O_q complete: the last O_q += P V (commit)
     kBDrain = 21,   // drain after an abort (one commit per active issuer)
@@ -455,11 +455,11 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
 
     if (warp == 0) tmem_alloc(sTmem, 512);
     if (tid == 0) {
-        // A stage is free again after the 128 converter threads (its V tile is
-        // widened) and one arrival per softmax warp of each active query tile (at
-        // the end of its tile: its S MMAs are done and its scale rows read).
-        const int kve = 128 + 4 * nq;
-        const int counts[L::kBars] = {1, 1, 1, 1, kve, kve, kve, 1,  1,  1,  1, 4, 4, 4, 4, 128, 128,
+        // A stage is free again after the four converter warps (its V tile is
+        // widened) and each softmax warp of each active query tile (at the end of
+        // its tile: its S MMAs are done and its scale rows read).
+        const int kve = 4 + 4 * nq;   // per stage: one arrival per converter warp and per softmax warp
+        const int counts[L::kBars] = {1, 1, 1, 1, kve, kve, kve, 1,  1,  1,  1, 4, 4, 4, 4, 4, 4,
                                       nq, nq, 1,  1,  nq, 4, 4, 4, 1, 1, 1, 1,  4, 4, 4, 4};
         for (int b = 0; b < L::kBars; ++b) mbar_init(&bars[b], counts[b]);
         fence_mbar_init();
@@ -682,9 +682,11 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                         make_uint4(h16[4], h16[5], h16[6], h16[7]);
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(&bars[kBVF + b]);
+                __syncwarp();
+                mbar_arrive_warp(&bars[kBVF + b]);
             }
-            mbar_arrive(&bars[kBKVE + st]);
+            __syncwarp();
+            mbar_arrive_warp(&bars[kBKVE + st]);
         }
     } else if (warp == 12) {
         // ------------------------------------------------------------ TMA producer
@@ -696,13 +698,13 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
             prefetch_tmap(&maps.vt8);
         }
         for (int ld = 0; ld < 2 * nt; ++ld) {
-            if (ld == (nt < NST ? nt : NST) && lane == 0) {
+            if (ld == (nt < NST ? nt : NST)) {
                 // the query tiles, once the first stages are on their way and Q prep
                 // (the grid before this one) has finished
                 asm volatile("griddepcontrol.wait;" ::: "memory");
-                mbar_expect_tx(&bars[kBQ], (uint32_t)(nq * L::kQ));
-                tma_load_3d(sQ, &maps.q8, &bars[kBQ], 0, (2 * pair) * 128, h);
-                if (nq == 2) tma_load_3d(sQ + L::kQ, &maps.q8, &bars[kBQ], 0, (2 * pair + 1) * 128, h);
+                mbar_expect_tx_warp(&bars[kBQ], (uint32_t)(nq * L::kQ));
+                tma_load_3d_warp(sQ, &maps.q8, &bars[kBQ], 0, (2 * pair) * 128, h);
+                if (nq == 2) tma_load_3d_warp(sQ + L::kQ, &maps.q8, &bars[kBQ], 0, (2 * pair + 1) * 128, h);
                 q_issued = true;
             }
             const int st = ld % NST;
@@ -710,15 +712,15 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                 break;
             const int j = j0 + ld % nt;
             const bool second = ld >= nt;
-            if (lane == 0 && j != p.skip_tile) {
-                mbar_expect_tx(&bars[kBKVF + st], (uint32_t)(L::kK + L::kAmRows + (second ? L::kV : 0)));
-                tma_load_3d(sK + st * L::kK, &maps.k8, &bars[kBKVF + st], 0, j * 128, zrow);
-                if (second) tma_load_3d(sV + st * L::kV, &maps.vt8, &bars[kBKVF + st], j * 128, 0, zrow);
-                bulk_g2s(sAm + st * L::kAm, kam + (size_t)j * 128, 512, &bars[kBKVF + st]);
-                bulk_g2s(sAm + st * L::kAm + 512, vam + (size_t)j * 128, 512, &bars[kBKVF + st]);
+            if (j != p.skip_tile) {
+                // the whole warp issues (elected lane)
+                mbar_expect_tx_warp(&bars[kBKVF + st], (uint32_t)(L::kK + L::kAmRows + (second ? L::kV : 0)));
+                tma_load_3d_warp(sK + st * L::kK, &maps.k8, &bars[kBKVF + st], 0, j * 128, zrow);
+                if (second) tma_load_3d_warp(sV + st * L::kV, &maps.vt8, &bars[kBKVF + st], j * 128, 0, zrow);
+                bulk_g2s_warp(sAm + st * L::kAm, kam + (size_t)j * 128, 512, &bars[kBKVF + st]);
+                bulk_g2s_warp(sAm + st * L::kAm + 512, vam + (size_t)j * 128, 512, &bars[kBKVF + st]);
                 issued[st]++;
             }
-            __syncwarp();
         }
     } else if (warp == 13 || warp == 14) {
         // ------------------------------------------------------------ MMA issuers
