@@ -146,7 +146,7 @@ enum : int {
     kBPF1 = 29,     // [2][2] first pass: that S read out (one arrival per softmax warp)
 };
 enum : int { kWaitQ = 1, kWaitKVFull = 2, kWaitKVEmpty = 3, kWaitS = 4, kWaitP = 5, kWaitO = 6, kWaitV16Full = 7,
-             kWaitV16Empty = 8 };
+             kWaitV16Empty = 8, kWaitMerge = 9 };
 constexpr int kAttendThreads = 512;
 constexpr int kMaxSplits = 4;   // KV splits per (head, query pair); the merge holds them all in registers
 
@@ -869,29 +869,60 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
         }
         if (lane == 0) *reinterpret_cast<float2*>(p.part_ml + pr * 2) = sML[rr];
     }
-    // Split merge.  Every CTA counts itself in, aborted or not, so the per-(head,
-    // pair) counter is back at zero after every call; the last split of the
-    // (head, query pair) to arrive merges all partials, one warp per row, four
-    // rows per warp at a time with all their loads in flight.
+    // Split merge.  Every CTA counts itself in, aborted or not.  Cooperative launch
+    // (all CTAs resident at once): the splits of a (head, pair) wait for each
+    // other (bounded) and each merges its share of the rows; a second counter
+    // tells the last one out to reset both.  Otherwise the last split to arrive
+    // merges all rows.  Either way one warp per row, four rows per warp at a
+    // time with all their loads in flight.
     __threadfence();
     __syncthreads();
-    int* counter = p.counters + (size_t)h * (p.Tstride / 256) + pair;
-    if (tid == 0) *sLast = atomicAdd(counter, 1) == p.splits - 1;
-    __syncthreads();
-    if (!*sLast) return;
-    __threadfence();
+    const size_t unit = (size_t)h * (p.Tstride / 256) + pair;
+    int* counter = p.counters + unit;
+    int* done = p.counters + (size_t)p.H * (p.Tstride / 256) + unit;
+    int r0 = 0, r1 = rows;
+    if (p.coop) {
+        if (tid == 0) {
+            atomicAdd(counter, 1);
+            const uint64_t t0 = globaltimer_ns();
+            int ok = 1;
+            while (atomicAdd(counter, 0) < p.splits) {
+                if ((long long)(globaltimer_ns() - t0) > p.timeout_ns) {
+                    ok = 0;
+                    if (atomicCAS(p.err, 0, KVRING_ETIMEOUT) == 0) {
+                        p.err[1] = kKernelAttend;
+                        p.err[2] = kWaitMerge;
+                        p.err[3] = (int)blockIdx.x;
+                    }
+                    break;
+                }
+            }
+            *sLast = ok;
+        }
+        __syncthreads();
+        r0 = split * rows / p.splits;
+        r1 = (split + 1) * rows / p.splits;
+        if (!*sLast) r1 = r0;   // gave up: merge nothing
+        __threadfence();
+    } else {
+        if (tid == 0) *sLast = atomicAdd(counter, 1) == p.splits - 1;
+        __syncthreads();
+        if (!*sLast) return;
+        __threadfence();
+    }
     constexpr int kRowsAtOnce = 4;
-    for (int rb = warp * kRowsAtOnce; rb < rows; rb += kRowsAtOnce * (kAttendThreads / 32)) {
+    for (int rb = r0 + warp * kRowsAtOnce; rb < r1; rb += kRowsAtOnce * (kAttendThreads / 32)) {
         float2 ml[kRowsAtOnce][kMaxSplits];
         float4 o[kRowsAtOnce][kMaxSplits];
 #pragma unroll
         for (int k = 0; k < kRowsAtOnce; ++k) {
             const int t = pair * 256 + rb + k;
+            const bool mine = rb + k < r1 && t < p.T;
 #pragma unroll
             for (int sp = 0; sp < kMaxSplits; ++sp) {
                 ml[k][sp] = make_float2(-INFINITY, 0.f);
                 o[k][sp] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (sp < p.splits && t < p.T) {
+                if (sp < p.splits && mine) {
                     const size_t pr = ((size_t)sp * p.H + h) * p.Tstride + t;
                     ml[k][sp] = __ldcg(reinterpret_cast<const float2*>(p.part_ml + pr * 2));
                     if (lanes_d) o[k][sp] = __ldcg(reinterpret_cast<const float4*>(p.part_o + pr * D + 4 * lane));
@@ -901,7 +932,7 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
 #pragma unroll
         for (int k = 0; k < kRowsAtOnce; ++k) {
             const int t = pair * 256 + rb + k;
-            if (t >= p.T || !lanes_d) continue;
+            if (rb + k >= r1 || t >= p.T || !lanes_d) continue;
             float mx = ml[k][0].x;
 #pragma unroll
             for (int sp = 1; sp < kMaxSplits; ++sp) mx = fmaxf(mx, ml[k][sp].x);
@@ -921,7 +952,16 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                 make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
         }
     }
-    if (tid == 0) *counter = 0;
+    if (p.coop) {
+        // the last split out resets both counters (every split has passed its wait)
+        __syncthreads();
+        if (tid == 0 && atomicAdd(done, 1) == p.splits - 1) {
+            *counter = 0;
+            *done = 0;
+        }
+    } else if (tid == 0) {
+        *counter = 0;
+    }
 }
 
 // Launched with programmatic stream serialisation: its CTAs may start while the
@@ -938,11 +978,13 @@ cudaError_t launch_attend(const AttendParams& p, const AttendMaps& maps, cudaStr
     cfg.blockDim = dim3(kAttendThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;   // the splits of a (head, pair) wait for each other
+    attr[1].val.cooperative = p.coop ? 1 : 0;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, p, maps);
 }
 

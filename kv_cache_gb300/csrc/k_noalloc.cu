@@ -164,6 +164,7 @@ extern "C" int kvring_attend_noalloc(const void* k8, const void* vt8, const floa
     ap.log2e_rsqrt_d = (float)(1.4426950408889634 / std::sqrt((double)d));
     ap.timeout_ns = 2000000000LL;
     ap.skip_tile = -1;
+    ap.coop = 0;
 
     e = launch_qprep(qp, s);
     if (e == cudaSuccess) e = launch_attend(ap, maps, s);

@@ -52,7 +52,7 @@ struct kvring {
     float* qamax = nullptr;     // [H][Tstride]
     float* part_o = nullptr;    // [max_splits][H][Tstride][d]
     float* part_ml = nullptr;   // [max_splits][H][Tstride][2]
-    int* counters = nullptr;    // [H][Tstride/256] split arrivals per (head, query pair)
+    int* counters = nullptr;    // [2][H][Tstride/256] split arrivals (and merges done) per (head, query pair)
     int* err = nullptr;         // [4]
     AttendMaps maps{};
     // testing aid
@@ -214,7 +214,7 @@ int kvring_create(const kvring_config* cfg_in, kvring_t** out) {
         {(void**)&r->q8, (size_t)(H * r->Tstride * d)}, {(void**)&r->qamax, (size_t)(H * r->Tstride) * sizeof(float)},
         {(void**)&r->part_o, (size_t)(r->max_splits * H * r->Tstride * d) * sizeof(float)},
         {(void**)&r->part_ml, (size_t)(r->max_splits * H * r->Tstride * 2) * sizeof(float)},
-        {(void**)&r->counters, (size_t)(H * npairs_max) * sizeof(int)},
+        {(void**)&r->counters, (size_t)(2 * H * npairs_max) * sizeof(int)},
         {(void**)&r->err, 4 * sizeof(int)},
     };
     for (auto& a : allocs) {
@@ -375,6 +375,8 @@ int kvring_attend(kvring_t* r, int32_t layer, const void* q, int32_t n_q, float*
     ap.log2e_rsqrt_d = (float)(1.4426950408889634 / std::sqrt((double)d));
     ap.timeout_ns = r->debug_timeout_ns > 0 ? r->debug_timeout_ns : 2000000000LL;
     ap.skip_tile = r->debug_skip_tile;
+    // with every CTA resident at once (one per SM), the splits merge together
+    ap.coop = (ap.splits > 1 && H * ap.npairs * ap.splits <= r->num_sms) ? 1 : 0;
     r->debug_skip_tile = -1;
     r->debug_timeout_ns = 0;
     e = launch_attend(ap, r->maps, s);
@@ -478,15 +480,15 @@ int kvring_check_device(kvring_t* r, void* stream) {
     if (e != cudaSuccess) return cuda_fail(r, e, "reading the device error word");
     if (w[0] == 0) return KVRING_OK;
     static const char* sites[] = {"?", "Q tiles", "K/V stage full", "K/V stage free", "S", "P", "O", "fp16 V full",
-                                  "fp16 V free"};
-    const int site = (w[2] >= 0 && w[2] <= 8) ? w[2] : 0;
+                                  "fp16 V free", "the other KV splits"};
+    const int site = (w[2] >= 0 && w[2] <= 9) ? w[2] : 0;
     const char* kernel = w[1] == 2 ? "write" : "attention";
     r->error = std::string("device wait timed out in the ") + kernel + " kernel (wait for " +
                (w[1] == 2 ? "input rows" : sites[site]) + ", block " + std::to_string(w[3]) + ")";
     e = cudaMemset(r->err, 0, sizeof(w));
     // a CTA that gave up may have left a split counter behind
     if (e == cudaSuccess)
-        e = cudaMemset(r->counters, 0, (size_t)r->cfg.num_heads * (r->Tstride / 256) * sizeof(int));
+        e = cudaMemset(r->counters, 0, 2 * (size_t)r->cfg.num_heads * (r->Tstride / 256) * sizeof(int));
     if (e != cudaSuccess) return cuda_fail(r, e, "clearing the device error word");
     return KVRING_ETIMEOUT;
 }

@@ -68,7 +68,7 @@ struct AttendParams {
     float* out;               // fp32 [T][H][d]
     float* part_o;            // fp32 [splits][H][Tstride][d]   (splits > 1)
     float* part_ml;           // fp32 [splits][H][Tstride][2]   (splits > 1)
-    int* counters;            // [H][Tstride/256], zero between calls (splits > 1)
+    int* counters;            // [2][H][Tstride/256], zero between calls (splits > 1)
     int* err;                 // device error word
     int T, H, d, Rpad, Tstride;
     int count;                // valid slots
@@ -80,6 +80,7 @@ struct AttendParams {
     float log2e_rsqrt_d;      // log2(e) / sqrt(d)
     long long timeout_ns;
     int skip_tile;            // testing aid: K/V load of this tile is not issued (-1 = off)
+    int coop;                 // launched cooperatively: the splits of a (head, pair) merge together
 };
 struct AttendMaps {
     CUtensorMap q8;           // 3-D {d, Tstride, H}
