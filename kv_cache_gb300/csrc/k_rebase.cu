@@ -19,8 +19,13 @@ namespace kvring_impl {
 
 constexpr int kRebaseThreads = 256;
 
+// Each thread handles kItems 16-byte pieces of a unit and issues every load
+// (the codes, their slots' amax, the rotation entries -- one RoPE table row per
+// layer, read through L1) before it uses any, so a unit costs one memory round
+// trip; no shared memory and no barriers.
+constexpr int kItems = 4;
+
 __global__ void __launch_bounds__(kRebaseThreads) rebase_kernel(const __grid_constant__ RebaseParams p) {
-    __shared__ float2 s_cs[64];
     const int d = p.d;
     const int c16n = d / 16;
     const int nsb = p.Rpad / 128;
@@ -33,37 +38,46 @@ __global__ void __launch_bounds__(kRebaseThreads) rebase_kernel(const __grid_con
         const int delta = p.delta[l];
         const int cnt = p.count[l];
         if (delta == 0 || sb * 128 >= cnt) continue;     // uniform over the block
-        __syncthreads();                                   // previous unit done with s_cs
-        if (tid < d / 2) {
-            const float2 cs = p.rope[(size_t)delta * (d / 2) + tid];
-            s_cs[tid] = make_float2(cs.x, -cs.y);          // rotation by -delta
-        }
-        __syncthreads();
         const int nslots = min(128, cnt - sb * 128);
         uint8_t* base = p.k8 + ((size_t)lh * p.Rpad + (size_t)sb * 128) * d;
         const float* am = p.kamax + (size_t)lh * p.Rpad + (size_t)sb * 128;
-#pragma unroll 2
-        for (int q = tid; q < nslots * c16n; q += kRebaseThreads) {
+        const float4* rot = reinterpret_cast<const float4*>(p.rope + (size_t)delta * (d / 2));   // (cos, sin) pairs
+        uint4 w[kItems];
+        float amax[kItems];
+        float4 cs[kItems][4];
+        bool live[kItems];
+#pragma unroll
+        for (int k = 0; k < kItems; ++k) {
+            const int q = tid + k * kRebaseThreads;
             const int r = q / c16n, c = q - r * c16n;
-            uint4* ptr = reinterpret_cast<uint4*>(base + (size_t)r * d + c * 16);
-            const uint4 w = *ptr;
-            const float amax = __ldg(am + r);
-            const float sc = scale_of(amax), iv = inv_of(amax);
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            live[k] = r < nslots;
+            if (live[k]) {
+                w[k] = *reinterpret_cast<const uint4*>(base + (size_t)r * d + c * 16);
+                amax[k] = __ldg(am + r);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) cs[k][e] = __ldg(rot + c * 4 + e);   // pairs 8c + 2e, 8c + 2e + 1
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kItems; ++k) {
+            if (!live[k]) continue;
+            const int q = tid + k * kRebaseThreads;
+            const int r = q / c16n, c = q - r * c16n;
+            const float sc = scale_of(amax[k]), iv = inv_of(amax[k]);
+            const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
             uint32_t out[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float2 f0 = e4m3x2_to_float2(ws[e] & 0xFFFFu);
                 const float2 f1 = e4m3x2_to_float2(ws[e] >> 16);
-                const float2 c0 = s_cs[c * 8 + 2 * e];
-                const float2 c1 = s_cs[c * 8 + 2 * e + 1];
                 float y0, y1, z0, z1;
-                rope_pair(__fmul_rn(f0.x, sc), __fmul_rn(f0.y, sc), c0.x, c0.y, y0, y1);
-                rope_pair(__fmul_rn(f1.x, sc), __fmul_rn(f1.y, sc), c1.x, c1.y, z0, z1);
+                // rotation by -delta: cos unchanged, sine negated
+                rope_pair(__fmul_rn(f0.x, sc), __fmul_rn(f0.y, sc), cs[k][e].x, -cs[k][e].y, y0, y1);
+                rope_pair(__fmul_rn(f1.x, sc), __fmul_rn(f1.y, sc), cs[k][e].z, -cs[k][e].w, z0, z1);
                 out[e] = e4m3x2(__fmul_rn(y0, iv), __fmul_rn(y1, iv)) |
                          (e4m3x2(__fmul_rn(z0, iv), __fmul_rn(z1, iv)) << 16);
             }
-            *ptr = make_uint4(out[0], out[1], out[2], out[3]);
+            *reinterpret_cast<uint4*>(base + (size_t)r * d + c * 16) = make_uint4(out[0], out[1], out[2], out[3]);
         }
     }
 }
