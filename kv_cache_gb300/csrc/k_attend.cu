@@ -40,8 +40,10 @@ namespace kvring_impl {
 // Rows T..Tpad-1 are written as zeros.
 __global__ void __launch_bounds__(128) qprep_kernel(const __grid_constant__ QPrepParams p) {
     // the attention kernel that follows may start its own set-up (it waits for
-    // this grid before it touches Q)
+    // this grid before it touches Q); this grid itself may have started before
+    // the one ahead of it finished, so it waits for it before reading anything
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int d = p.d;
     const int tpr = d / 8;                       // threads per row, 8 elements each
     const int rows_per_block = 128 / tpr;
@@ -79,11 +81,21 @@ __global__ void __launch_bounds__(128) qprep_kernel(const __grid_constant__ QPre
     }
 }
 
+// Launched with programmatic stream serialisation (its launch overlaps the tail
+// of the grid before it; it waits for that grid before reading anything).
 cudaError_t launch_qprep(const QPrepParams& p, cudaStream_t s) {
     const int rows_per_block = 128 / (p.d / 8);
     const int rows = p.H * p.Tpad;
-    qprep_kernel<<<(rows + rows_per_block - 1) / rows_per_block, 128, 0, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)((rows + rows_per_block - 1) / rows_per_block), 1, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, qprep_kernel, p);
 }
 
 
@@ -440,6 +452,9 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+    // the grid after this one may be scheduled as SMs free up (it waits for this
+    // one before it reads or writes anything)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     int u = blockIdx.x;
     const int split = u % p.splits;

@@ -17,15 +17,16 @@
 
 namespace kvring_impl {
 
-constexpr int kRebaseThreads = 256;
 
-// Each thread handles kItems 16-byte pieces of a unit and issues every load
-// (the codes, their slots' amax, the rotation entries -- one RoPE table row per
-// layer, read through L1) before it uses any, so a unit costs one memory round
-// trip; no shared memory and no barriers.
-constexpr int kItems = 4;
+// Each thread handles kItems 16-byte pieces of a unit, all in the same column
+// chunk (the block's thread count is a multiple of the chunks per row), and
+// issues every load (the codes, their slots' amax, the chunk's rotation entries
+// -- one RoPE table row per layer, read through L1) before it uses any, so a
+// unit costs one memory round trip; no shared memory and no barriers.
+constexpr int kItems = 8;
+constexpr int kRebaseThreadsR = 128;   // threads per block; 128 * kItems = 1024 pieces = one 128-slot unit at d = 128
 
-__global__ void __launch_bounds__(kRebaseThreads) rebase_kernel(const __grid_constant__ RebaseParams p) {
+__global__ void __launch_bounds__(kRebaseThreadsR) rebase_kernel(const __grid_constant__ RebaseParams p) {
     const int d = p.d;
     const int c16n = d / 16;
     const int nsb = p.Rpad / 128;
@@ -42,27 +43,26 @@ __global__ void __launch_bounds__(kRebaseThreads) rebase_kernel(const __grid_con
         uint8_t* base = p.k8 + ((size_t)lh * p.Rpad + (size_t)sb * 128) * d;
         const float* am = p.kamax + (size_t)lh * p.Rpad + (size_t)sb * 128;
         const float4* rot = reinterpret_cast<const float4*>(p.rope + (size_t)delta * (d / 2));   // (cos, sin) pairs
+        const int c = tid % c16n;   // this thread's column chunk, the same for all its pieces
+        float4 cs[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) cs[e] = __ldg(rot + c * 4 + e);   // pairs 8c + 2e, 8c + 2e + 1
         uint4 w[kItems];
         float amax[kItems];
-        float4 cs[kItems][4];
         bool live[kItems];
 #pragma unroll
         for (int k = 0; k < kItems; ++k) {
-            const int q = tid + k * kRebaseThreads;
-            const int r = q / c16n, c = q - r * c16n;
+            const int r = (tid + k * kRebaseThreadsR) / c16n;
             live[k] = r < nslots;
             if (live[k]) {
                 w[k] = *reinterpret_cast<const uint4*>(base + (size_t)r * d + c * 16);
                 amax[k] = __ldg(am + r);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) cs[k][e] = __ldg(rot + c * 4 + e);   // pairs 8c + 2e, 8c + 2e + 1
             }
         }
 #pragma unroll
         for (int k = 0; k < kItems; ++k) {
             if (!live[k]) continue;
-            const int q = tid + k * kRebaseThreads;
-            const int r = q / c16n, c = q - r * c16n;
+            const int r = (tid + k * kRebaseThreadsR) / c16n;
             const float sc = scale_of(amax[k]), iv = inv_of(amax[k]);
             const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
             uint32_t out[4];
@@ -72,8 +72,8 @@ __global__ void __launch_bounds__(kRebaseThreads) rebase_kernel(const __grid_con
                 const float2 f1 = e4m3x2_to_float2(ws[e] >> 16);
                 float y0, y1, z0, z1;
                 // rotation by -delta: cos unchanged, sine negated
-                rope_pair(__fmul_rn(f0.x, sc), __fmul_rn(f0.y, sc), cs[k][e].x, -cs[k][e].y, y0, y1);
-                rope_pair(__fmul_rn(f1.x, sc), __fmul_rn(f1.y, sc), cs[k][e].z, -cs[k][e].w, z0, z1);
+                rope_pair(__fmul_rn(f0.x, sc), __fmul_rn(f0.y, sc), cs[e].x, -cs[e].y, y0, y1);
+                rope_pair(__fmul_rn(f1.x, sc), __fmul_rn(f1.y, sc), cs[e].z, -cs[e].w, z0, z1);
                 out[e] = e4m3x2(__fmul_rn(y0, iv), __fmul_rn(y1, iv)) |
                          (e4m3x2(__fmul_rn(z0, iv), __fmul_rn(z1, iv)) << 16);
             }
@@ -84,10 +84,10 @@ __global__ void __launch_bounds__(kRebaseThreads) rebase_kernel(const __grid_con
 
 cudaError_t launch_rebase(const RebaseParams& p, int num_sms, cudaStream_t s) {
     const long long units = (long long)p.L * p.H * (p.Rpad / 128);
-    long long grid = (long long)num_sms * 8;
+    long long grid = (long long)num_sms * 16;
     if (grid > units) grid = units;
     if (grid < 1) grid = 1;
-    rebase_kernel<<<(unsigned)grid, kRebaseThreads, 0, s>>>(p);
+    rebase_kernel<<<(unsigned)grid, kRebaseThreadsR, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -71,6 +71,11 @@ __global__ void __launch_bounds__(kWriteThreads) write_kernel(const __grid_const
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_bar)) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    // This grid may start before the one ahead of it in the stream has finished
+    // (programmatic launch): the set-up above overlaps that grid's tail, and
+    // nothing is read or written before it has finished.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     __syncthreads();
     const uint16_t* src = is_v ? p.v : p.k;
     if (tid < 32) {
@@ -217,13 +222,15 @@ cudaError_t launch_write(const WriteParams& p, cudaStream_t s) {
     cfg.blockDim = dim3(kWriteThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, write_kernel, p);
 }
 
