@@ -120,6 +120,7 @@ def run_gpu(args, cfg, rank, world):
     torch.cuda.set_device(device)
     kv.load()
     L, H, d, R, T, P, RE = (cfg[k] for k in ("L", "H", "d", "R", "T", "passes", "reset_every"))
+    WP = cfg["writes_per_step"]           # 1, or P when every pass rewrites the newest chunk
     ring = kv.KVRing(L, H, d, R, T, max_position=R + RE * T)
     host, pool = make_pool(cfg, torch, device)
     stream = torch.cuda.current_stream(device)
@@ -139,14 +140,17 @@ def run_gpu(args, cfg, rank, world):
                 timers["n_rebase"] += 1
         for p in range(P):
             for l in range(L):
-                if p == 0:
-                    i = synthetic.pool_index(s, l, 4, L)
-                    k = inputs["k"][l] if inputs else pool["k"][i]
-                    v = inputs["v"][l] if inputs else pool["v"][i]
+                if p < WP:
+                    i = synthetic.pool_index(s, l, 4 if p == 0 else p, L)
+                    k = inputs["k"][p * L + l] if inputs else pool["k"][i]
+                    v = inputs["v"][p * L + l] if inputs else pool["v"][i]
                     if timers is not None:
                         ev = timers["write"][timers["nw"]]
                         ev[0].record(stream)
-                    ring.write(l, k, v, stream=stream)
+                    if p == 0:
+                        ring.write(l, k, v, stream=stream)
+                    else:
+                        ring.rewrite(l, k, v, stream=stream)
                     if timers is not None:
                         ev[1].record(stream)
                         timers["nw"] += 1
@@ -170,7 +174,7 @@ def run_gpu(args, cfg, rank, world):
 
     K = args.steps
     mk = lambda: torch.cuda.Event(enable_timing=True)
-    timers = {"write": [(mk(), mk()) for _ in range(K * L)], "attend": [(mk(), mk()) for _ in range(K * L * P)],
+    timers = {"write": [(mk(), mk()) for _ in range(K * L * WP)], "attend": [(mk(), mk()) for _ in range(K * L * P)],
               "rebase": (mk(), mk()), "nw": 0, "na": 0, "n_rebase": 0}
     launches0 = ring.launch_count()
     sampler = ClockSampler(device.index)
@@ -199,8 +203,8 @@ def run_gpu(args, cfg, rank, world):
     # ---- end to end: host inputs (pinned) -> device, attention outputs -> host, every step
     e2e_steps = max(1, min(K, args.e2e_steps))
     pin = {r: [torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).pin_memory() for b in host[r]] for r in host}
-    dev_in = {"k": [torch.empty((T, H, d), dtype=torch.bfloat16, device=device) for _ in range(L)],
-              "v": [torch.empty((T, H, d), dtype=torch.bfloat16, device=device) for _ in range(L)],
+    dev_in = {"k": [torch.empty((T, H, d), dtype=torch.bfloat16, device=device) for _ in range(L * WP)],
+              "v": [torch.empty((T, H, d), dtype=torch.bfloat16, device=device) for _ in range(L * WP)],
               "q": [torch.empty((T, H, d), dtype=torch.bfloat16, device=device) for _ in range(L * P)]}
     host_out = [torch.empty((T, H, d), dtype=torch.float32).pin_memory() for _ in range(P)]
     h2d = d2h = 0
@@ -210,12 +214,13 @@ def run_gpu(args, cfg, rank, world):
     for _ in range(e2e_steps):
         s = step_counter[0]
         for l in range(L):
-            i = synthetic.pool_index(s, l, 4, L)
-            dev_in["k"][l].copy_(pin["k"][i], non_blocking=True)
-            dev_in["v"][l].copy_(pin["v"][i], non_blocking=True)
+            for p in range(WP):
+                i = synthetic.pool_index(s, l, 4 if p == 0 else p, L)
+                dev_in["k"][p * L + l].copy_(pin["k"][i], non_blocking=True)
+                dev_in["v"][p * L + l].copy_(pin["v"][i], non_blocking=True)
             for p in range(P):
                 dev_in["q"][p * L + l].copy_(pin["q"][synthetic.pool_index(s, l, p, L)], non_blocking=True)
-        h2d += (2 * L + P * L) * T * H * d * 2
+        h2d += (2 * L * WP + P * L) * T * H * d * 2
         one_step(inputs=dev_in)
         for p in range(P):
             host_out[p].copy_(outs[p], non_blocking=True)
@@ -242,15 +247,19 @@ def oracle_sample(cfg, seconds_hint=20.0):
     qs = [f32(synthetic.chunk("q", p, T, H, d, True)) for p in range(P)]
     k = f32(synthetic.chunk("k", fill, T, H, d, True))
     v = f32(synthetic.chunk("v", fill, T, H, d, True))
+    WP = cfg.get("writes_per_step", 1)
     t0 = time.perf_counter()
     naive.write(k, v)
     for p in range(P):
+        if 0 < p < WP:
+            naive.rewrite(k, v)
         naive.attend(qs[p])
     block_s = time.perf_counter() - t0
     step_s = block_s * L
     threads = os.cpu_count()
     return dict(block_s=block_s, step_s=step_s, cores=threads,
-                sample=f"one block (1 write + {P} attention calls, naive per-call upkeep, float64 attention) "
+                sample=f"one block (1 write + {WP - 1} rewrites + {P} attention calls, naive per-call upkeep, "
+                       f"float64 attention) "
                        f"at {H} heads x {d}, R={R}, T={T}; x{L} blocks (extrapolated)")
 
 
@@ -271,8 +280,13 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--small", action="store_true", help="4 blocks instead of 60 (quick checks)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rewrite-per-pass", action="store_true",
+                    help="passes 1..3 rewrite the newest chunk with new K/V (kvring_write_ex, no advance)")
     args = ap.parse_args()
-    cfg = SMALL if args.small else WORKLOAD
+    cfg = dict(SMALL if args.small else WORKLOAD)
+    cfg["writes_per_step"] = cfg["passes"] if args.rewrite_per_pass else 1
+    if args.rewrite_per_pass:
+        cfg["name"] = cfg["name"].replace("(1 write + 4 attention calls)", "(1 write + 3 rewrites + 4 attention calls)")
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     L, H, d, R, T, P = (cfg[k] for k in ("L", "H", "d", "R", "T", "passes"))
@@ -334,7 +348,8 @@ def main():
                      "kernel": "attention call (q-prep + attention + split combine)",
                      "peak_source": f"{peak_src}: 2 x bf16_tflops_sustained (FP8 = 2 x bf16 nominal ratio)"},
         "breakdown": {
-            "upkeep_ms_per_step": w_avg * L, "upkeep_gbs": write_gbs,
+            "upkeep_ms_per_step": w_avg * L * cfg["writes_per_step"], "upkeep_gbs": write_gbs,
+            "writes_per_block_per_step": cfg["writes_per_step"],
             "upkeep_frac_hbm": write_gbs / peaks["hbm_gbs"],
             "write_us_per_call": w_avg * 1e3,
             "attend_us_per_call": a_avg * 1e3, "attend_tflops_per_call": attn_tflops,

@@ -106,6 +106,26 @@ int kvring_destroy(kvring_t* ring);
 int kvring_write(kvring_t* ring, int32_t layer, const void* k_bf16, const void* v_bf16,
                  int32_t n_tokens, void* cuda_stream);
 
+/* Flags of kvring_write_ex. */
+#define KVRING_WRITE_REWRITE 0x1u   /* replace the latest chunk instead of appending one */
+
+/* kvring_write with flags.  flags == 0 is kvring_write.
+ * KVRING_WRITE_REWRITE: the latest chunk of `layer` is written again with new K, V
+ * and nothing advances.  A denoising model runs every block several times per
+ * step ([ai.info] "La gestione della cache...": four passes through the 60
+ * blocks, 240 attention calls per step), and the newest chunk's K and V are new
+ * on each pass; the pages do not say how the cache takes them, and this call is
+ * the plain reading: the same slots (head - n_tokens ... head - 1) mod R, the same
+ * positions (last_write_pos + j, after any rebase since), the same chunk id, and
+ * a new frozen scale per (head, chunk) from the new amax.  head, count,
+ * next_pos and the write counter do not change; attend keeps reading the chunk
+ * as the latest one.  Slots of older chunks are never touched.
+ * Errors: as kvring_write, plus EINVAL (unknown flag bits) and ESTATE (rewrite
+ * before any write to the layer, or n_tokens != the latest write's n_tokens;
+ * n_tokens == 0 is a no-op only without the flag). */
+int kvring_write_ex(kvring_t* ring, int32_t layer, const void* k_bf16, const void* v_bf16,
+                    int32_t n_tokens, uint32_t flags, void* cuda_stream);
+
 /* Attention of the latest chunk's queries over the finished FP8 cache of `layer`
  * ([wechild] paragraph 6; [ai.info] "Latenza dei turni...": FP8 attention that
  * accepts per-head scales).

@@ -7,4 +7,5 @@ Build with ``python -m kv_cache_gb300.build``.
 from .kvring import (KVRING_EINVAL, KVRING_ENODEV, KVRING_ENOMEM, KVRING_ECUDA, KVRING_ESTATE,  # noqa: F401
                      KVRING_ETIMEOUT, KVRING_OK, KVRing, KVRingError, kvring_attend, kvring_attend_noalloc, kvring_check_device,
                      kvring_config, kvring_create, kvring_debug_fault, kvring_destroy, kvring_get_state,
-                     kvring_last_error, kvring_launch_count, kvring_rebase, kvring_snapshot, kvring_state, kvring_write)
+                     kvring_last_error, kvring_launch_count, kvring_rebase, kvring_snapshot, kvring_state, kvring_write,
+                     kvring_write_ex, KVRING_WRITE_REWRITE)

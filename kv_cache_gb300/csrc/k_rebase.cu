@@ -83,9 +83,12 @@ __global__ void __launch_bounds__(kRebaseThreadsR) rebase_kernel(const __grid_co
 }
 
 cudaError_t launch_rebase(const RebaseParams& p, int num_sms, cudaStream_t s) {
+    // one unit per block: the blocks in flight then cover one contiguous stretch of
+    // the rings (measured faster than a persistent or grid-stride layout)
+    (void)num_sms;
     const long long units = (long long)p.L * p.H * (p.Rpad / 128);
-    long long grid = (long long)num_sms * 16;
-    if (grid > units) grid = units;
+    long long grid = units;
+    if (grid > 0x7fffffffLL) grid = 0x7fffffffLL;
     if (grid < 1) grid = 1;
     rebase_kernel<<<(unsigned)grid, kRebaseThreadsR, 0, s>>>(p);
     return cudaGetLastError();

@@ -53,6 +53,7 @@ struct kvring {
     float* part_o = nullptr;    // [max_splits][H][Tstride][d]
     float* part_ml = nullptr;   // [max_splits][H][Tstride][2]
     int* counters = nullptr;    // [2][H][Tstride/256] split arrivals (and merges done) per (head, query pair)
+    float* wpart = nullptr;     // [2][amax blocks][H] per-block amax partials of the write kernels
     int* err = nullptr;         // [4]
     AttendMaps maps{};
     // testing aid
@@ -74,13 +75,15 @@ int cuda_fail(kvring_t* r, cudaError_t e, const char* what) {
 }
 
 void free_device(kvring_t* r) {
-    void* ptrs[] = {r->k8, r->vt8, r->kamax, r->vamax, r->rope, r->q8, r->qamax, r->part_o, r->part_ml, r->counters, r->err};
+    void* ptrs[] = {r->k8, r->vt8, r->kamax, r->vamax, r->rope, r->q8, r->qamax, r->part_o, r->part_ml, r->counters,
+                    r->wpart, r->err};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     r->k8 = r->vt8 = r->q8 = nullptr;
     r->kamax = r->vamax = r->qamax = r->part_o = r->part_ml = nullptr;
     r->rope = nullptr;
     r->counters = nullptr;
+    r->wpart = nullptr;
     r->err = nullptr;
 }
 
@@ -215,6 +218,9 @@ int kvring_create(const kvring_config* cfg_in, kvring_t** out) {
         {(void**)&r->part_o, (size_t)(r->max_splits * H * r->Tstride * d) * sizeof(float)},
         {(void**)&r->part_ml, (size_t)(r->max_splits * H * r->Tstride * 2) * sizeof(float)},
         {(void**)&r->counters, (size_t)(2 * H * npairs_max) * sizeof(int)},
+        {(void**)&r->wpart, (size_t)(2 * H) * sizeof(float) *
+                                (size_t)((cfg.max_tokens_per_write + write_amax_tokens_per_block((int)H, (int)d) - 1) /
+                                         write_amax_tokens_per_block((int)H, (int)d))},
         {(void**)&r->err, 4 * sizeof(int)},
     };
     for (auto& a : allocs) {
@@ -260,17 +266,25 @@ int kvring_destroy(kvring_t* r) {
     return KVRING_OK;
 }
 
-int kvring_write(kvring_t* r, int32_t layer, const void* k, const void* v, int32_t n, void* stream) {
+int kvring_write_ex(kvring_t* r, int32_t layer, const void* k, const void* v, int32_t n,
+                    uint32_t flags, void* stream) {
     if (!r) return KVRING_EINVAL;
     const kvring_config& c = r->cfg;
     if (layer < 0 || layer >= c.num_layers) return fail(r, KVRING_EINVAL, "layer out of range");
+    if (flags & ~KVRING_WRITE_REWRITE) return fail(r, KVRING_EINVAL, "unknown write flag");
     if (n < 0 || n > c.max_tokens_per_write) return fail(r, KVRING_EINVAL, "n_tokens out of range [0, max_tokens_per_write]");
+    LayerState& L = r->layers[layer];
+    const bool rewrite = (flags & KVRING_WRITE_REWRITE) != 0;
+    if (rewrite && L.writes == 0) return fail(r, KVRING_ESTATE, "rewrite before any write to this layer");
+    if (rewrite && n != L.last_n) return fail(r, KVRING_ESTATE, "a rewrite must have the latest write's n_tokens");
     if (n == 0) return KVRING_OK;
     if (!r->host_only && (!k || !v)) return fail(r, KVRING_EINVAL, "k or v is NULL");
-    LayerState& L = r->layers[layer];
-    if (L.next_pos + n > c.max_position)
+    if (!rewrite && L.next_pos + n > c.max_position)
         return fail(r, KVRING_ESTATE, "positions would reach max_position: call kvring_rebase first");
     const int R = c.capacity;
+    // first slot and position of the chunk written: the next ones, or the latest chunk's again
+    const int64_t slot0 = rewrite ? (L.head - n + R) % R : L.head;
+    const int64_t pos0 = rewrite ? L.last_pos : L.next_pos;
     if (!r->host_only) {
         WriteParams p{};
         p.k = static_cast<const uint16_t*>(k);
@@ -281,31 +295,34 @@ int kvring_write(kvring_t* r, int32_t layer, const void* k, const void* v, int32
         p.kamax = r->kamax + lh * r->Rpad;
         p.vamax = r->vamax + lh * r->Rpad;
         p.rope = r->rope;
-        p.head = L.head;
-        p.pos0 = L.next_pos;
+        p.head = slot0;
+        p.pos0 = pos0;
         p.T = n;
         p.H = c.num_heads;
         p.d = c.head_dim;
         p.R = R;
         p.Rpad = (int)r->Rpad;
         p.ngroups_ring = (R + 15) / 16;
-        p.group0 = (int)(L.head / 16);
-        // 16-slot groups touched by slots [head, head + n) mod R
-        const int64_t end = L.head + n;
+        p.group0 = (int)(slot0 / 16);
+        // 16-slot groups touched by slots [slot0, slot0 + n) mod R
+        const int64_t end = slot0 + n;
         int groups;
         if (end <= R) {
-            groups = (int)((end - 1) / 16 - L.head / 16 + 1);
+            groups = (int)((end - 1) / 16 - slot0 / 16 + 1);
         } else {
-            const int64_t g1 = p.ngroups_ring - L.head / 16;
+            const int64_t g1 = p.ngroups_ring - slot0 / 16;
             const int64_t g2 = (end - R - 1) / 16 + 1;
             groups = (int)std::min<int64_t>(p.ngroups_ring, g1 + g2);
         }
         p.groups = groups;
-        p.err = r->err;
+        p.amax_tokens_per_block = write_amax_tokens_per_block(p.H, p.d);
+        p.amax_blocks = (n + p.amax_tokens_per_block - 1) / p.amax_tokens_per_block;
+        p.part = r->wpart;
         cudaError_t e = launch_write(p, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(r, e, "write kernel launch");
-        r->launches += 1;
+        r->launches += 2;
     }
+    if (rewrite) return KVRING_OK;   // same slots, positions and chunk id: nothing moves
     for (int j = 0; j < n; ++j) {
         const int64_t slot = (L.head + j) % R;
         L.pos[slot] = (int32_t)(L.next_pos + j);
@@ -318,6 +335,10 @@ int kvring_write(kvring_t* r, int32_t layer, const void* k, const void* v, int32
     L.next_pos += n;
     L.writes += 1;
     return KVRING_OK;
+}
+
+int kvring_write(kvring_t* r, int32_t layer, const void* k, const void* v, int32_t n, void* stream) {
+    return kvring_write_ex(r, layer, k, v, n, 0u, stream);
 }
 
 int kvring_attend(kvring_t* r, int32_t layer, const void* q, int32_t n_q, float* out, void* stream) {
@@ -482,9 +503,8 @@ int kvring_check_device(kvring_t* r, void* stream) {
     static const char* sites[] = {"?", "Q tiles", "K/V stage full", "K/V stage free", "S", "P", "O", "fp16 V full",
                                   "fp16 V free", "the other KV splits"};
     const int site = (w[2] >= 0 && w[2] <= 9) ? w[2] : 0;
-    const char* kernel = w[1] == 2 ? "write" : "attention";
-    r->error = std::string("device wait timed out in the ") + kernel + " kernel (wait for " +
-               (w[1] == 2 ? "input rows" : sites[site]) + ", block " + std::to_string(w[3]) + ")";
+    r->error = std::string("device wait timed out in the attention kernel (wait for ") + sites[site] +
+               ", block " + std::to_string(w[3]) + ")";
     e = cudaMemset(r->err, 0, sizeof(w));
     // a CTA that gave up may have left a split counter behind
     if (e == cudaSuccess)

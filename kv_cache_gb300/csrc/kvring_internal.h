@@ -16,7 +16,7 @@ constexpr float kE4M3Max = 448.0f;
 
 // Device error word: [0] = status (0 or KVRING_ETIMEOUT), [1] = kernel id,
 // [2] = wait site, [3] = block index that gave up.
-enum KernelId : int { kKernelAttend = 1, kKernelWrite = 2 };
+enum KernelId : int { kKernelAttend = 1 };
 
 // ---------------------------------------------------------------- write (K1)
 struct WriteParams {
@@ -33,9 +33,12 @@ struct WriteParams {
     int groups;               // 16-slot groups touched by the chunk
     int group0;               // first group in cyclic order
     int ngroups_ring;         // ceil(R / 16)
-    int* err;                 // device error word
+    int amax_tokens_per_block;
+    int amax_blocks;          // ceil(T / amax_tokens_per_block)
+    float* part;              // per-block amax partials [K|V][amax_blocks][H] (ring scratch)
 };
-cudaError_t launch_write(const WriteParams& p, cudaStream_t s);
+cudaError_t launch_write(const WriteParams& p, cudaStream_t s);   // two launches
+int write_amax_tokens_per_block(int H, int d);
 
 // ---------------------------------------------------------------- rebase (K2)
 struct RebaseParams {

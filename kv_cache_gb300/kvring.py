@@ -75,6 +75,7 @@ _SIGNATURES = {
     "kvring_create": (ctypes.c_int, [ctypes.POINTER(kvring_config), ctypes.POINTER(_P)]),
     "kvring_destroy": (ctypes.c_int, [_P]),
     "kvring_write": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P, ctypes.c_int32, _P]),
+    "kvring_write_ex": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P, ctypes.c_int32, ctypes.c_uint32, _P]),
     "kvring_attend": (ctypes.c_int, [_P, ctypes.c_int32, _P, ctypes.c_int32, _P, _P]),
     "kvring_rebase": (ctypes.c_int, [_P, _P]),
     "kvring_get_state": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.POINTER(kvring_state)]),
@@ -148,6 +149,16 @@ def kvring_write(ring, layer: int, k, v, n_tokens: int, H: int, d: int, stream=N
     vp = _dev_bf16(v, n_tokens, H, d, "v") if v is not None else None
     s = _stream(stream) if (k is not None or v is not None) else 0
     _check(load().kvring_write(ring, layer, kp, vp, n_tokens, s), ring)
+
+
+KVRING_WRITE_REWRITE = 0x1
+
+
+def kvring_write_ex(ring, layer: int, k, v, n_tokens: int, flags: int, H: int, d: int, stream=None) -> None:
+    kp = _dev_bf16(k, n_tokens, H, d, "k") if k is not None else None
+    vp = _dev_bf16(v, n_tokens, H, d, "v") if v is not None else None
+    s = _stream(stream) if (k is not None or v is not None) else 0
+    _check(load().kvring_write_ex(ring, layer, kp, vp, n_tokens, flags, s), ring)
 
 
 def kvring_attend(ring, layer: int, q, n_q: int, out, H: int, d: int, stream=None) -> None:
@@ -262,6 +273,11 @@ class KVRing:
     def write(self, layer: int, k, v, n_tokens: Optional[int] = None, stream=None) -> None:
         n = k.shape[0] if n_tokens is None else n_tokens
         kvring_write(self.handle, layer, k, v, n, self.H, self.d, stream)
+
+    def rewrite(self, layer: int, k, v, n_tokens: Optional[int] = None, stream=None) -> None:
+        """Replace the latest chunk of ``layer`` with new K, V (next denoise pass)."""
+        n = k.shape[0] if n_tokens is None else n_tokens
+        kvring_write_ex(self.handle, layer, k, v, n, KVRING_WRITE_REWRITE, self.H, self.d, stream)
 
     def attend(self, layer: int, q, out=None, stream=None):
         import torch

@@ -156,6 +156,19 @@ class NaiveWindow:
         self.tokens += T
         self.writes += 1
 
+    def rewrite(self, k: np.ndarray, v: np.ndarray) -> None:
+        """The next denoise pass's k, v for the latest chunk: its rows (the newest T of
+        the window) take the new values and the chunk its new amax; nothing shifts."""
+        k = np.asarray(k, F32)
+        v = np.asarray(v, F32)
+        T = k.shape[0]
+        assert self.writes > 0 and T == self.last_n
+        c = self.writes - 1
+        self.kamax[c] = chunk_amax_k(k)
+        self.vamax[c] = chunk_amax_v(v)
+        self.k[-T:] = k
+        self.v[-T:] = v
+
     def rebase(self) -> int:
         delta = self.next_pos - self.count
         self.pos = self.pos - delta
@@ -221,6 +234,35 @@ class WriteTimeRing:
         assert 0 < T <= self.R
         slots = (self.head + np.arange(T)) % self.R
         pos = self.next_pos + np.arange(T, dtype=np.int64)
+        self._store(k, v, slots, pos, self.writes)
+        self.last_pos, self.last_n = self.next_pos, T
+        self.head = (self.head + T) % self.R
+        self.count = min(self.count + T, self.R)
+        self.next_pos += T
+        self.writes += 1
+        return slots
+
+    def rewrite(self, k: np.ndarray, v: np.ndarray) -> np.ndarray:
+        """The next denoise pass's k, v [T][H][d] for the latest chunk; returns its slots.
+
+        The model runs its blocks four times per step and each pass makes new K
+        and V for the newest chunk (ai.info, "La gestione della cache spostata al
+        momento della scrittura": four passes, 240 attention calls per step).  The
+        pages say nothing more; the plain reading: the same slots, positions and
+        chunk id as the latest write, a new per-head scale from the new amax, and
+        no change to head, count, next_pos or the write counter.
+        """
+        k = np.asarray(k, F32)
+        v = np.asarray(v, F32)
+        T = k.shape[0]
+        assert self.writes > 0 and T == self.last_n
+        slots = (self.head - T + np.arange(T)) % self.R
+        pos = self.last_pos + np.arange(T, dtype=np.int64)
+        self._store(k, v, slots, pos, self.writes - 1)
+        return slots
+
+    def _store(self, k, v, slots, pos, chunk_id):
+        """RoPE K at ``pos``, quantise K and V with this chunk's scales, store at ``slots``."""
         ka = chunk_amax_k(k)
         va = chunk_amax_v(v)
         _, ki = scale_inv(ka)
@@ -233,13 +275,7 @@ class WriteTimeRing:
         self.kamax[:, slots] = ka[:, None]
         self.vamax[:, slots] = va[:, None]
         self.pos[slots] = pos
-        self.chunk[slots] = self.writes
-        self.last_pos, self.last_n = self.next_pos, T
-        self.head = (self.head + T) % self.R
-        self.count = min(self.count + T, self.R)
-        self.next_pos += T
-        self.writes += 1
-        return slots
+        self.chunk[slots] = chunk_id
 
     def rebase(self) -> int:
         """Delta-rotate every cached K by -delta in place; returns delta."""

@@ -116,3 +116,45 @@ def test_null_handles_are_rejected():
     assert lib.kvring_rebase(None, None) == kv.KVRING_EINVAL
     assert lib.kvring_destroy(None) == kv.KVRING_OK
     assert lib.kvring_get_state(None, 0, None) == kv.KVRING_EINVAL
+
+
+@pytest.mark.parametrize("R,T", [(96, 32), (100, 32), (5788, 757), (7, 7)])
+def test_rewrite_passes_leave_the_schedule_unchanged(R, T):
+    # one write and three rewrites per step, resets every 42 steps: the state
+    # after each call equals the oracle's
+    ring = _ring(1, 1, 64, R, T, max_position=R + 42 * T)
+    o = WriteTimeRing(R, 1, 2)
+    z = np.zeros((T, 1, 2), np.float32)
+    for s in range(90):
+        if s > 0 and s % 42 == 0:
+            ring.rebase()
+            o.rebase()
+        ring.write(0, None, None, n_tokens=T)
+        o.write(z, z)
+        for _ in range(3):
+            ring.rewrite(0, None, None, n_tokens=T)
+            o.rewrite(z, z)
+            _compare(ring, 0, o)
+
+
+def test_rewrite_errors_leave_state_unchanged():
+    ring = _ring(1, 2, 64, 96, 32, max_position=200)
+    lib = kv.load()
+    with pytest.raises(kv.KVRingError) as e:
+        ring.rewrite(0, None, None, n_tokens=32)
+    assert e.value.code == kv.KVRING_ESTATE and "before any write" in e.value.message
+    ring.write(0, None, None, n_tokens=20)
+    before = ring.state(0)
+    for n in (19, 21, 0):
+        with pytest.raises(kv.KVRingError) as e:
+            ring.rewrite(0, None, None, n_tokens=n)
+        assert e.value.code == kv.KVRING_ESTATE and "n_tokens" in e.value.message
+    assert lib.kvring_write_ex(ring.handle, 0, None, None, 20, 0x2, None) == kv.KVRING_EINVAL
+    assert "flag" in kv.kvring_last_error(ring.handle)
+    assert ring.state(0) == before
+    for _ in range(8):                          # next_pos = 180: a rewrite never checks max_position
+        ring.write(0, None, None, n_tokens=20)
+    ring.rewrite(0, None, None, n_tokens=20)
+    assert ring.state(0)["next_pos"] == 180 and ring.state(0)["last_write_pos"] == 160
+    assert lib.kvring_write_ex(ring.handle, 0, None, None, 21, 0, None) == kv.KVRING_ESTATE   # 201 > 200
+    assert lib.kvring_write_ex(None, 0, None, None, 1, 1, None) == kv.KVRING_EINVAL

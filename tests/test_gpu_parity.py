@@ -154,6 +154,57 @@ def test_rebase_many_layers_production_heads():
         assert fk == 1.0 and fv == 1.0
 
 
+@pytest.mark.parametrize("R,T,H,d", [(96, 32, 2, 64), (100, 32, 2, 128), (300, 100, 3, 128), (40, 40, 1, 64)])
+def test_rewrite_passes_small(R, T, H, d):
+    """Four denoise passes per step: one write, then three rewrites of the same chunk."""
+    ring = kv.KVRing(1, H, d, R, T, max_position=4096)
+    o = WriteTimeRing(R, H, d)
+    for w in range(2 * R // T + 2):
+        for p in range(4):
+            i = 4 * w + p
+            kb, kf = chunk_pair("k", 500 + i, T, H, d, p % 2 == 1)
+            vb, vf = chunk_pair("v", 500 + i, T, H, d, p % 2 == 1)
+            if p == 0:
+                ring.write(0, to_dev(kb), to_dev(vb))
+                o.write(kf, vf)
+            else:
+                ring.rewrite(0, to_dev(kb), to_dev(vb))
+                o.rewrite(kf, vf)
+            fk, fv = _check_cache(ring, 0, o)
+            assert fk == 1.0 and fv == 1.0
+            qb, qf = chunk_pair("q", 500 + i, T, H, d, True)
+            out = ring.attend(0, to_dev(qb)).cpu().numpy()
+            assert_attention_close(out, o.attend(qf), f"write {w} pass {p}")
+
+
+def test_rewrite_after_reset_production_sampled():
+    """Production shape: the ring wraps, positions reset, then passes 1..3 rewrite the
+    latest chunk at its shifted positions; cache bytes and sampled attention."""
+    R, T, H, d = 5788, 757, 16, 128
+    ring = kv.KVRing(1, H, d, R, T, max_position=R + 42 * T)
+    o = WriteTimeRing(R, H, d)
+    for w in range(9):
+        kb, kf = chunk_pair("k", 700 + w, T, H, d, True)
+        vb, vf = chunk_pair("v", 700 + w, T, H, d, True)
+        ring.write(0, to_dev(kb), to_dev(vb))
+        o.write(kf, vf)
+    ring.rebase()
+    assert o.rebase() > 0
+    rng = np.random.default_rng(11)
+    heads = np.array([0, 7, 15])
+    rows = np.unique(np.concatenate([rng.choice(T, 40, replace=False), [0, 127, 128, 756]]))
+    for p in range(1, 4):
+        kb, kf = chunk_pair("k", 720 + p, T, H, d, True)
+        vb, vf = chunk_pair("v", 720 + p, T, H, d, True)
+        ring.rewrite(0, to_dev(kb), to_dev(vb))
+        o.rewrite(kf, vf)
+        qb, qf = chunk_pair("q", 720 + p, T, H, d, True)
+        out = ring.attend(0, to_dev(qb)).cpu().numpy()
+        assert_attention_close(out[np.ix_(rows, heads)], o.attend(qf, heads=heads, rows=rows), f"pass {p}")
+    fk, fv = _check_cache(ring, 0, o)
+    assert fk == 1.0 and fv == 1.0
+
+
 def test_edge_sizes():
     # T = 1, T = R (whole ring in one write), then a write that wraps mid-group
     R, H, d = 40, 1, 64

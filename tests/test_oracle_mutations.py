@@ -82,6 +82,40 @@ class _RingOffByOne(schemes_mod.WriteTimeRing):
         return slots
 
 
+class _RewriteNextSlots(schemes_mod.WriteTimeRing):
+    # rewrite lands on the slots after the latest chunk instead of on it
+    def rewrite(self, k, v):
+        T = np.asarray(k).shape[0]
+        slots = (self.head + np.arange(T)) % self.R
+        pos = self.last_pos + np.arange(T, dtype=np.int64)
+        self._store(np.asarray(k, np.float32), np.asarray(v, np.float32), slots, pos, self.writes - 1)
+        return slots
+
+
+class _RewriteNextPositions(schemes_mod.WriteTimeRing):
+    # rewrite rotates K at next_pos (the positions of the chunk to come)
+    def rewrite(self, k, v):
+        T = np.asarray(k).shape[0]
+        slots = (self.head - T + np.arange(T)) % self.R
+        pos = self.next_pos + np.arange(T, dtype=np.int64)
+        self._store(np.asarray(k, np.float32), np.asarray(v, np.float32), slots, pos, self.writes - 1)
+        return slots
+
+
+class _RewriteStaleScale(schemes_mod.WriteTimeRing):
+    # rewrite keeps the first pass's K amax instead of taking the new chunk's
+    def rewrite(self, k, v):
+        T = np.asarray(k).shape[0]
+        slots = (self.head - T + np.arange(T)) % self.R
+        old = self.kamax[:, slots].copy()
+        super().rewrite(k, v)
+        _, ki = schemes_mod.scale_inv(old[:, 0])
+        kr = rope_mod.rotate_at(np.asarray(k, np.float32), self.last_pos + np.arange(T), self.d, self.theta)
+        self.k8[:, slots, :] = schemes_mod.quantise(kr, ki[None, :, None]).transpose(1, 0, 2)
+        self.kamax[:, slots] = old
+        return slots
+
+
 CASES = [
     ("rotation sign", [(rope_mod, "rotate", _rotate_sign_flipped)], t_rope.test_unit_vector_rotates_to_cos_sin),
     ("rotate-half pairing", [(rope_mod, "rotate", _rotate_halves)], t_rope.test_matches_complex_multiplication),
@@ -91,6 +125,9 @@ CASES = [
     ("softmax axis", [(t_att, "attention_fp64", _attention_transposed)], t_att.test_rows_are_convex_combinations_and_key_order_free),
     ("K amax not pair norm", [(t_sch, "chunk_amax_k", _amax_plain)], t_sch.test_amax_k_is_largest_pair_norm_bruteforce),
     ("ring head drift", [(t_ring, "WriteTimeRing", _RingOffByOne)], lambda: t_ring.test_logical_order_equals_shifted_window(96, 32)),
+    ("rewrite slots", [(t_ring, "WriteTimeRing", _RewriteNextSlots)], lambda: t_ring.test_rewrite_equals_writing_that_chunk(10, 4, 3)),
+    ("rewrite positions", [(t_ring, "WriteTimeRing", _RewriteNextPositions)], t_ring.test_rewrite_after_reset_uses_the_shifted_positions),
+    ("rewrite stale scale", [(t_ring, "WriteTimeRing", _RewriteStaleScale)], lambda: t_ring.test_rewrite_equals_writing_that_chunk(12, 4, 3)),
 ]
 
 

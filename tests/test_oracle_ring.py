@@ -111,3 +111,75 @@ def test_scale_frozen_through_eviction():
     from oracle.schemes import chunk_amax_k
     assert np.all(ring.kamax[:, 6] == chunk_amax_k(chunks[1]))
     assert np.all(ring.kamax[:, 7] == chunk_amax_k(chunks[1]))
+
+
+def _ring_arrays(r: WriteTimeRing):
+    return (r.k8, r.v8, r.kamax, r.vamax, r.pos, r.chunk)
+
+
+def _ring_counters(r: WriteTimeRing):
+    return (r.head, r.count, r.next_pos, r.writes, r.last_pos, r.last_n, r.resets)
+
+
+@pytest.mark.parametrize("R,T,nw", [(10, 4, 3), (10, 4, 5), (12, 4, 3), (7, 7, 2), (300, 100, 4)])
+def test_rewrite_equals_writing_that_chunk(R, T, nw):
+    # history c_0..c_{nw-2}, then c_{nw-1} written and replaced by x over 3 passes:
+    # the ring must equal the one that wrote x in c_{nw-1}'s place (nw = 3 at R = 10
+    # straddles the ring's end; R = 12 ends on it; T = R overwrites everything)
+    H, d = 2, 8
+    rng = np.random.default_rng(R * 131 + T * 7 + nw)
+    mk = lambda s: (rng.standard_normal((T, H, d)) * s).astype(np.float32)
+    hist = [(mk(w + 1), mk(w + 2)) for w in range(nw)]
+    passes = [(mk(3 + p), mk(0.5 + p)) for p in range(3)]
+    a, b = WriteTimeRing(R, H, d), WriteTimeRing(R, H, d)
+    for k, v in hist:
+        a.write(k, v)
+    for k, v in hist[:-1]:
+        b.write(k, v)
+    before = [x.copy() for x in _ring_arrays(a)]
+    counters = _ring_counters(a)
+    for k, v in passes:
+        slots = a.rewrite(k, v)
+        assert _ring_counters(a) == counters
+    b.write(*passes[-1])
+    assert list(slots) == list((b.head - T + np.arange(T)) % R)
+    for x, y in zip(_ring_arrays(a), _ring_arrays(b)):
+        assert np.array_equal(x, y)
+    assert _ring_counters(a) == _ring_counters(b)
+    # no slot outside the latest chunk moved
+    others = np.ones(R, bool)
+    others[slots] = False
+    for i, (x, y) in enumerate(zip(before, _ring_arrays(a))):
+        ax = 1 if i < 4 else 0                          # slot axis: [H][R](...), then [R]
+        assert np.array_equal(np.compress(others, x, axis=ax), np.compress(others, y, axis=ax))
+
+
+def test_rewrite_after_reset_uses_the_shifted_positions():
+    # after a reset the latest chunk sits at count - T; a rewrite there must code x
+    # exactly as a fresh ring that wrote x at that position
+    R, T, H, d = 12, 4, 2, 8
+    rng = np.random.default_rng(5)
+    a = WriteTimeRing(R, H, d)
+    for w in range(5):                                   # next_pos 20, count 12: delta 8
+        a.write(rng.standard_normal((T, H, d)).astype(np.float32), rng.standard_normal((T, H, d)).astype(np.float32))
+    assert a.rebase() == 8
+    assert a.last_pos == R - T
+    x = (rng.standard_normal((T, H, d)) * 3).astype(np.float32)
+    y = rng.standard_normal((T, H, d)).astype(np.float32)
+    slots = a.rewrite(x, y)
+    assert list(a.pos[slots]) == list(range(R - T, R))
+    b = WriteTimeRing(R, H, d)
+    b.write(np.ones((R - T, H, d), np.float32), np.ones((R - T, H, d), np.float32))
+    fresh = b.write(x, y)
+    assert np.array_equal(a.k8[:, slots], b.k8[:, fresh])
+    assert np.array_equal(a.v8[:, slots], b.v8[:, fresh])
+    assert np.array_equal(a.kamax[:, slots], b.kamax[:, fresh])
+
+
+def test_rewrite_needs_a_write_of_the_same_size():
+    r = WriteTimeRing(8, 1, 2)
+    with pytest.raises(AssertionError):
+        r.rewrite(_zeros(4), _zeros(4))
+    r.write(_zeros(4), _zeros(4))
+    with pytest.raises(AssertionError):
+        r.rewrite(_zeros(3), _zeros(3))

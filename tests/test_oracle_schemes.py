@@ -92,6 +92,29 @@ def test_writetime_equals_naive_before_reset(R, T, H, d):
             assert np.max(np.abs(a - b)) < 1e-12
 
 
+@pytest.mark.parametrize("R,T,H,d", [(96, 32, 2, 64), (100, 32, 2, 64), (8, 8, 1, 16)])
+def test_rewrite_passes_writetime_equals_naive(R, T, H, d):
+    # the two schemes hold the same codes after every denoise pass, including the
+    # passes that replace the latest chunk, and attend alike
+    naive = NaiveWindow(R, H, d)
+    ring = WriteTimeRing(R, H, d)
+    for w in range(2 * R // T + 2):
+        for p in range(4):
+            k = _chunk("k", 40 * w + p, T, H, d, outliers=p == 2)
+            v = _chunk("v", 40 * w + p, T, H, d, outliers=p == 3)
+            if p == 0:
+                naive.write(k, v)
+                ring.write(k, v)
+            else:
+                naive.rewrite(k, v)
+                ring.rewrite(k, v)
+            k8, v8, _, _ = naive.cache_codes()
+            assert np.array_equal(_logical(ring, ring.k8), k8.transpose(1, 0, 2))
+            assert np.array_equal(_logical(ring, ring.v8), v8.transpose(1, 0, 2))
+        q = _chunk("q", w, T, H, d)
+        assert np.max(np.abs(naive.attend(q) - ring.attend(q))) < 1e-12
+
+
 @pytest.mark.parametrize("R,T,H,d", [(96, 32, 2, 64), (100, 32, 2, 64)])
 def test_rebase_within_one_pair_step_of_fresh_rotation(R, T, H, d):
     naive = NaiveWindow(R, H, d)
