@@ -121,7 +121,8 @@ def run_gpu(args, cfg, rank, world):
     kv.load()
     L, H, d, R, T, P, RE = (cfg[k] for k in ("L", "H", "d", "R", "T", "passes", "reset_every"))
     WP = cfg["writes_per_step"]           # 1, or P when every pass rewrites the newest chunk
-    ring = kv.KVRing(L, H, d, R, T, max_position=R + RE * T)
+    NV = cfg.get("naive_upkeep", False)   # the comparison scheme: refresh the whole window per call
+    ring = kv.KVRing(L, H, d, R, T, max_position=R + RE * T, naive_upkeep=NV)
     host, pool = make_pool(cfg, torch, device)
     stream = torch.cuda.current_stream(device)
     outs = [torch.empty((T, H, d), dtype=torch.float32, device=device) for _ in range(P)]
@@ -154,6 +155,14 @@ def run_gpu(args, cfg, rank, world):
                     if timers is not None:
                         ev[1].record(stream)
                         timers["nw"] += 1
+                if NV:
+                    if timers is not None:
+                        ev = timers["refresh"][timers["nr"]]
+                        ev[0].record(stream)
+                    ring.naive_refresh(l, stream=stream)
+                    if timers is not None:
+                        ev[1].record(stream)
+                        timers["nr"] += 1
                 q = inputs["q"][p * L + l] if inputs else pool["q"][synthetic.pool_index(s, l, p, L)]
                 if timers is not None:
                     ev = timers["attend"][timers["na"]]
@@ -175,7 +184,8 @@ def run_gpu(args, cfg, rank, world):
     K = args.steps
     mk = lambda: torch.cuda.Event(enable_timing=True)
     timers = {"write": [(mk(), mk()) for _ in range(K * L * WP)], "attend": [(mk(), mk()) for _ in range(K * L * P)],
-              "rebase": (mk(), mk()), "nw": 0, "na": 0, "n_rebase": 0}
+              "rebase": (mk(), mk()), "nw": 0, "na": 0, "n_rebase": 0,
+              "refresh": [(mk(), mk()) for _ in range(K * L * P if NV else 0)], "nr": 0}
     launches0 = ring.launch_count()
     sampler = ClockSampler(device.index)
     if world > 1:
@@ -186,7 +196,7 @@ def run_gpu(args, cfg, rank, world):
     t0, t1 = mk(), mk()
     t0.record(stream)
     for _ in range(K):
-        one_step(timers)
+        one_step()                 # nothing but the path's own calls between t0 and t1
     t1.record(stream)
     torch.cuda.synchronize(device)
     clocks = sampler.stop()
@@ -196,8 +206,17 @@ def run_gpu(args, cfg, rank, world):
     if ring.check_device(stream) != kv.KVRING_OK:
         raise RuntimeError("device wait timed out during the timed region: " + kv.kvring_last_error(ring.handle))
     ms = t0.elapsed_time(t1)
+    # per-call breakdown: the same number of steps again, with an event pair around
+    # each call (events between calls keep consecutive kernels from overlapping, so
+    # these are taken apart from the step time above; K >= reset_every includes a reset)
+    for _ in range(K):
+        one_step(timers)
+    torch.cuda.synchronize(device)
+    if ring.check_device(stream) != kv.KVRING_OK:
+        raise RuntimeError("device wait timed out during the breakdown pass: " + kv.kvring_last_error(ring.handle))
     w_ms = [a.elapsed_time(b) for a, b in timers["write"][:timers["nw"]]]
     a_ms = [a.elapsed_time(b) for a, b in timers["attend"][:timers["na"]]]
+    r_ms = [a.elapsed_time(b) for a, b in timers["refresh"][:timers["nr"]]]
     rb_ms = timers["rebase"][0].elapsed_time(timers["rebase"][1]) if timers["n_rebase"] else None
 
     # ---- end to end: host inputs (pinned) -> device, attention outputs -> host, every step
@@ -229,7 +248,7 @@ def run_gpu(args, cfg, rank, world):
     torch.cuda.synchronize(device)
     e2e_ms = e0.elapsed_time(e1)
     ring.close()
-    return dict(ms=ms, w_ms=w_ms, a_ms=a_ms, rb_ms=rb_ms, launches=launches, clocks=clocks,
+    return dict(ms=ms, w_ms=w_ms, a_ms=a_ms, r_ms=r_ms, rb_ms=rb_ms, launches=launches, clocks=clocks,
                 e2e_ms=e2e_ms, e2e_steps=e2e_steps, h2d=h2d // e2e_steps, d2h=d2h // e2e_steps)
 
 
@@ -280,13 +299,20 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--small", action="store_true", help="4 blocks instead of 60 (quick checks)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--naive-upkeep", action="store_true",
+                    help="the comparison scheme: shift the bf16 window on write, re-rotate and re-quantise "
+                         "all of it before every attention call (kvring_naive_refresh)")
     ap.add_argument("--rewrite-per-pass", action="store_true",
                     help="passes 1..3 rewrite the newest chunk with new K/V (kvring_write_ex, no advance)")
     args = ap.parse_args()
     cfg = dict(SMALL if args.small else WORKLOAD)
     cfg["writes_per_step"] = cfg["passes"] if args.rewrite_per_pass else 1
+    cfg["naive_upkeep"] = bool(args.naive_upkeep)
     if args.rewrite_per_pass:
         cfg["name"] = cfg["name"].replace("(1 write + 4 attention calls)", "(1 write + 3 rewrites + 4 attention calls)")
+    if args.naive_upkeep:
+        cfg["name"] = cfg["name"].replace("attention calls)", "attention calls, each after a naive whole-window "
+                                          "re-rotation + re-quantisation; window shifted by copy on write)")
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     L, H, d, R, T, P = (cfg[k] for k in ("L", "H", "d", "R", "T", "passes"))
@@ -348,7 +374,9 @@ def main():
                      "kernel": "attention call (q-prep + attention + split combine)",
                      "peak_source": f"{peak_src}: 2 x bf16_tflops_sustained (FP8 = 2 x bf16 nominal ratio)"},
         "breakdown": {
-            "upkeep_ms_per_step": w_avg * L * cfg["writes_per_step"], "upkeep_gbs": write_gbs,
+            "upkeep_ms_per_step": w_avg * L * cfg["writes_per_step"] + (sum(r["r_ms"]) / K if r["r_ms"] else 0.0),
+            "upkeep_gbs": write_gbs,
+            "naive_refresh_us_per_call": (statistics.mean(r["r_ms"]) * 1e3) if r["r_ms"] else None,
             "writes_per_block_per_step": cfg["writes_per_step"],
             "upkeep_frac_hbm": write_gbs / peaks["hbm_gbs"],
             "write_us_per_call": w_avg * 1e3,

@@ -53,6 +53,19 @@ extern "C" {
  * write/rebase update the host state exactly as a device ring would; attend and
  * snapshot return KVRING_EINVAL.  Used to validate schedules on hosts without a GPU. */
 #define KVRING_FLAG_HOST_ONLY 0x1u
+/* The naive cache upkeep the pages replaced, kept as a measured comparison
+ * ([wechild] paragraph 7; [ai.info] "La gestione della cache...": before the
+ * change, cache upkeep took 69.7 ms of a 239.2 ms step).  Each layer holds its
+ * window as un-rotated bf16 K and V in logical order (oldest first) with each
+ * row's chunk amax.  kvring_write appends the chunk and drops the oldest rows
+ * by copying the window; a rewrite replaces the newest rows; kvring_rebase only
+ * lowers the positions.  kvring_naive_refresh re-applies RoPE to the whole window
+ * at its current positions and re-quantises K and V into the layer's FP8 cache
+ * (row r -> slot r), the upkeep the naive scheme repeats before every attention
+ * call; kvring_attend reads that cache.  Rows are never rotated twice, so the
+ * cache equals a fresh rotation at the current positions.  Uses 4 bytes per
+ * element more device memory than a write-time ring (two bf16 window copies). */
+#define KVRING_FLAG_NAIVE_UPKEEP 0x2u
 
 #define KVRING_MAX_LAYERS 256
 
@@ -137,6 +150,15 @@ int kvring_write_ex(kvring_t* ring, int32_t layer, const void* k_bf16, const voi
  * Errors: EINVAL, ESTATE (no write yet, n_q mismatch), ECUDA. */
 int kvring_attend(kvring_t* ring, int32_t layer, const void* q_bf16, int32_t n_q,
                   float* out_f32, void* cuda_stream);
+
+/* Naive per-call upkeep of one layer (rings created with KVRING_FLAG_NAIVE_UPKEEP):
+ * rows [0, count) of the bf16 window are rotated by RoPE at positions
+ * next_pos - count + r, quantised to e4m3 with their chunk scales (the same rules
+ * as kvring_write) and stored in slots [0, count) of the layer's FP8 cache with
+ * their chunk amax.  kvring_attend on a naive ring returns ESTATE unless the
+ * layer was refreshed after its latest write, rewrite or rebase.
+ * Errors: EINVAL (layer, or not a naive ring), ESTATE (no write yet), ECUDA. */
+int kvring_naive_refresh(kvring_t* ring, int32_t layer, void* cuda_stream);
 
 /* Position reset of every layer ([ai.info] "La gestione della cache...": positions
  * reset every 42 steps, one delta rotation of the cached window per reset).

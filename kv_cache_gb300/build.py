@@ -19,7 +19,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libkvring.so")
-SOURCES = ["kvring_api.cu", "k_write.cu", "k_rebase.cu", "k_attend.cu", "k_noalloc.cu"]
+SOURCES = ["kvring_api.cu", "k_write.cu", "k_rebase.cu", "k_attend.cu", "k_noalloc.cu", "k_naive.cu"]
 HEADERS = ["kvring_internal.h", "common.cuh", "tc.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "-I", os.path.join(ROOT, "include")]

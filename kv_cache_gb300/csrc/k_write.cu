@@ -212,10 +212,14 @@ int write_amax_tokens_per_block(int H, int d) {
     return per_token >= pieces ? 1 : pieces / per_token;
 }
 
-cudaError_t launch_write(const WriteParams& p, cudaStream_t s) {
+cudaError_t launch_write_amax(const WriteParams& p, cudaStream_t s) {
     const dim3 g1((unsigned)p.amax_blocks, 2);
-    cudaError_t e = launch_pdl(reinterpret_cast<const void*>(write_amax_kernel), g1, dim3(kAmaxThreads),
-                               (size_t)p.H * sizeof(uint32_t), s, p);
+    return launch_pdl(reinterpret_cast<const void*>(write_amax_kernel), g1, dim3(kAmaxThreads),
+                      (size_t)p.H * sizeof(uint32_t), s, p);
+}
+
+cudaError_t launch_write(const WriteParams& p, cudaStream_t s) {
+    cudaError_t e = launch_write_amax(p, s);
     if (e != cudaSuccess) return e;
     const dim3 g2((unsigned)p.groups, (unsigned)p.H, 2);
     return launch_pdl(reinterpret_cast<const void*>(write_store_kernel), g2, dim3(kStoreThreads), 0, s, p);

@@ -24,6 +24,8 @@ namespace {
 
 struct LayerState {
     int64_t head = 0, count = 0, next_pos = 0, writes = 0, last_pos = 0, last_n = 0;
+    int cur = 0;                  // naive upkeep: which window buffer holds the window
+    bool fresh = false;           // naive upkeep: FP8 cache refreshed since the last change
     std::vector<int32_t> pos;     // [R], -1 = empty
     std::vector<int32_t> chunk;   // [R], -1 = empty
 };
@@ -37,6 +39,7 @@ int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 struct kvring {
     kvring_config cfg{};
     bool host_only = false;
+    bool naive = false;         // KVRING_FLAG_NAIVE_UPKEEP
     int device = 0, num_sms = 0;
     int64_t Rpad = 0, Tstride = 0;
     int max_splits = 1;
@@ -54,6 +57,10 @@ struct kvring {
     float* part_ml = nullptr;   // [max_splits][H][Tstride][2]
     int* counters = nullptr;    // [2][H][Tstride/256] split arrivals (and merges done) per (head, query pair)
     float* wpart = nullptr;     // [2][amax blocks][H] per-block amax partials of the write kernels
+    uint16_t* kwin = nullptr;   // naive upkeep: bf16 windows [2 buffers][L][H][Rpad][d]
+    uint16_t* vwin = nullptr;
+    float* kaw = nullptr;       // naive upkeep: chunk amax of each window row [2][L][H][Rpad]
+    float* vaw = nullptr;
     int* err = nullptr;         // [4]
     AttendMaps maps{};
     // testing aid
@@ -76,7 +83,7 @@ int cuda_fail(kvring_t* r, cudaError_t e, const char* what) {
 
 void free_device(kvring_t* r) {
     void* ptrs[] = {r->k8, r->vt8, r->kamax, r->vamax, r->rope, r->q8, r->qamax, r->part_o, r->part_ml, r->counters,
-                    r->wpart, r->err};
+                    r->wpart, r->kwin, r->vwin, r->kaw, r->vaw, r->err};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     r->k8 = r->vt8 = r->q8 = nullptr;
@@ -84,6 +91,8 @@ void free_device(kvring_t* r) {
     r->rope = nullptr;
     r->counters = nullptr;
     r->wpart = nullptr;
+    r->kwin = r->vwin = nullptr;
+    r->kaw = r->vaw = nullptr;
     r->err = nullptr;
 }
 
@@ -137,7 +146,7 @@ int check_config(const kvring_config* c) {
         return fail(nullptr, KVRING_EINVAL, "max_tokens_per_write out of range [1, min(capacity, 2048)]");
     if (c->max_position < 0) return fail(nullptr, KVRING_EINVAL, "max_position must be >= 0");
     if (c->rope_theta < 0 || !std::isfinite(c->rope_theta)) return fail(nullptr, KVRING_EINVAL, "rope_theta must be finite and >= 0");
-    if (c->flags & ~KVRING_FLAG_HOST_ONLY) return fail(nullptr, KVRING_EINVAL, "unknown flag bits");
+    if (c->flags & ~(KVRING_FLAG_HOST_ONLY | KVRING_FLAG_NAIVE_UPKEEP)) return fail(nullptr, KVRING_EINVAL, "unknown flag bits");
     return KVRING_OK;
 }
 
@@ -153,6 +162,77 @@ int choose_splits(const kvring_t* r, int units, int ntiles) {
         if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = se; }
     }
     return best;
+}
+
+// Write or rewrite on a naive-upkeep ring (arguments already checked): the window
+// is shifted by a copy (write) or its newest rows replaced (rewrite); positions
+// and chunk ids of the window rows are kept in logical order.
+int naive_write(kvring_t* r, int layer, const void* k, const void* v, int n, bool rewrite, void* stream) {
+    const kvring_config& c = r->cfg;
+    LayerState& L = r->layers[layer];
+    const int R = c.capacity;
+    const int64_t drop = rewrite ? 0 : std::max<int64_t>(0, L.count + n - R);
+    const int64_t keep = rewrite ? L.count - n : L.count - drop;
+    if (!r->host_only) {
+        const int H = c.num_heads, d = c.head_dim;
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        WriteParams w{};
+        w.k = static_cast<const uint16_t*>(k);
+        w.v = static_cast<const uint16_t*>(v);
+        w.T = n;
+        w.H = H;
+        w.d = d;
+        w.amax_tokens_per_block = write_amax_tokens_per_block(H, d);
+        w.amax_blocks = (n + w.amax_tokens_per_block - 1) / w.amax_tokens_per_block;
+        w.part = r->wpart;
+        cudaError_t e = launch_write_amax(w, s);
+        if (e != cudaSuccess) return cuda_fail(r, e, "write amax kernel launch");
+        const size_t win = (size_t)H * r->Rpad * d, am = (size_t)H * r->Rpad;
+        const size_t per_buf = (size_t)c.num_layers;
+        const int src = L.cur, dst = rewrite ? L.cur : 1 - L.cur;
+        NaiveAppendParams p{};
+        p.k = w.k;
+        p.v = w.v;
+        p.kw_src = r->kwin + (src * per_buf + layer) * win;
+        p.vw_src = r->vwin + (src * per_buf + layer) * win;
+        p.kw_dst = r->kwin + (dst * per_buf + layer) * win;
+        p.vw_dst = r->vwin + (dst * per_buf + layer) * win;
+        p.ka_src = r->kaw + (src * per_buf + layer) * am;
+        p.va_src = r->vaw + (src * per_buf + layer) * am;
+        p.ka_dst = r->kaw + (dst * per_buf + layer) * am;
+        p.va_dst = r->vaw + (dst * per_buf + layer) * am;
+        p.part = r->wpart;
+        p.amax_blocks = w.amax_blocks;
+        p.T = n;
+        p.H = H;
+        p.d = d;
+        p.Rpad = (int)r->Rpad;
+        p.keep = (int)keep;
+        p.drop = (int)drop;
+        p.row_begin = rewrite ? (int)keep : 0;
+        e = launch_naive_append(p, s);
+        if (e != cudaSuccess) return cuda_fail(r, e, "naive append kernel launch");
+        r->launches += 2;
+        L.cur = dst;
+    }
+    L.fresh = false;
+    if (rewrite) return KVRING_OK;
+    // window rows in logical order: the kept rows move up by `drop`, the chunk follows
+    for (int64_t row = 0; row < keep; ++row) {
+        L.pos[row] = L.pos[row + drop];
+        L.chunk[row] = L.chunk[row + drop];
+    }
+    for (int j = 0; j < n; ++j) {
+        L.pos[keep + j] = (int32_t)(L.next_pos + j);
+        L.chunk[keep + j] = (int32_t)L.writes;
+    }
+    L.last_pos = L.next_pos;
+    L.last_n = n;
+    L.count = keep + n;
+    L.head = L.count % R;
+    L.next_pos += n;
+    L.writes += 1;
+    return KVRING_OK;
 }
 
 }  // namespace
@@ -185,6 +265,7 @@ int kvring_create(const kvring_config* cfg_in, kvring_t** out) {
     if (!r) return fail(nullptr, KVRING_ENOMEM, "host allocation failed");
     r->cfg = cfg;
     r->host_only = (cfg.flags & KVRING_FLAG_HOST_ONLY) != 0;
+    r->naive = (cfg.flags & KVRING_FLAG_NAIVE_UPKEEP) != 0;
     r->Rpad = round_up(cfg.capacity, 128);
     r->Tstride = round_up(cfg.max_tokens_per_write, 256);
     r->layers.resize(cfg.num_layers);
@@ -223,6 +304,19 @@ int kvring_create(const kvring_config* cfg_in, kvring_t** out) {
                                          write_amax_tokens_per_block((int)H, (int)d))},
         {(void**)&r->err, 4 * sizeof(int)},
     };
+    const size_t win_bytes = r->naive ? 2 * ring_bytes * sizeof(uint16_t) : 0;
+    const size_t winam_bytes = r->naive ? 2 * amax_bytes : 0;
+    struct { void** p; size_t n; } naive_allocs[] = {
+        {(void**)&r->kwin, win_bytes}, {(void**)&r->vwin, win_bytes},
+        {(void**)&r->kaw, winam_bytes}, {(void**)&r->vaw, winam_bytes},
+    };
+    for (auto& a : naive_allocs) {
+        if (a.n == 0) continue;
+        e = cudaMalloc(a.p, a.n);
+        if (e != cudaSuccess) { free_device(r); delete r; return fail(nullptr, KVRING_ENOMEM, std::string("cudaMalloc: ") + cudaGetErrorString(e)); }
+        e = cudaMemset(*a.p, 0, a.n);
+        if (e != cudaSuccess) { free_device(r); delete r; return fail(nullptr, KVRING_ECUDA, std::string("cudaMemset: ") + cudaGetErrorString(e)); }
+    }
     for (auto& a : allocs) {
         e = cudaMalloc(a.p, a.n);
         if (e != cudaSuccess) { free_device(r); delete r; return fail(nullptr, KVRING_ENOMEM, std::string("cudaMalloc: ") + cudaGetErrorString(e)); }
@@ -281,6 +375,7 @@ int kvring_write_ex(kvring_t* r, int32_t layer, const void* k, const void* v, in
     if (!r->host_only && (!k || !v)) return fail(r, KVRING_EINVAL, "k or v is NULL");
     if (!rewrite && L.next_pos + n > c.max_position)
         return fail(r, KVRING_ESTATE, "positions would reach max_position: call kvring_rebase first");
+    if (r->naive) return naive_write(r, layer, k, v, n, rewrite, stream);
     const int R = c.capacity;
     // first slot and position of the chunk written: the next ones, or the latest chunk's again
     const int64_t slot0 = rewrite ? (L.head - n + R) % R : L.head;
@@ -352,6 +447,8 @@ int kvring_attend(kvring_t* r, int32_t layer, const void* q, int32_t n_q, float*
     const LayerState& L = r->layers[layer];
     if (L.writes == 0 || L.count == 0) return fail(r, KVRING_ESTATE, "attend before any write to this layer");
     if (n_q != L.last_n) return fail(r, KVRING_ESTATE, "n_q must equal the latest write's n_tokens");
+    if (r->naive && !L.fresh)
+        return fail(r, KVRING_ESTATE, "naive-upkeep ring: kvring_naive_refresh is due after a write, rewrite or rebase");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int d = c.head_dim, H = c.num_heads;
     const int Tpad = (int)round_up(n_q, 128);
@@ -418,7 +515,7 @@ int kvring_rebase(kvring_t* r, void* stream) {
         p.count[l] = (int)L.count;
         any = any || (delta != 0 && L.count > 0);
     }
-    if (!r->host_only && any) {
+    if (!r->host_only && any && !r->naive) {   // a naive ring rotates at every refresh instead
         p.k8 = r->k8;
         p.kamax = r->kamax;
         p.rope = r->rope;
@@ -438,8 +535,43 @@ int kvring_rebase(kvring_t* r, void* stream) {
                 if (ps >= 0) ps -= (int32_t)delta;
         L.last_pos -= delta;
         L.next_pos = L.count;
+        if (delta != 0) L.fresh = false;
     }
     r->resets += 1;
+    return KVRING_OK;
+}
+
+int kvring_naive_refresh(kvring_t* r, int32_t layer, void* stream) {
+    if (!r) return KVRING_EINVAL;
+    const kvring_config& c = r->cfg;
+    if (!r->naive) return fail(r, KVRING_EINVAL, "not a naive-upkeep ring (KVRING_FLAG_NAIVE_UPKEEP)");
+    if (layer < 0 || layer >= c.num_layers) return fail(r, KVRING_EINVAL, "layer out of range");
+    LayerState& L = r->layers[layer];
+    if (L.writes == 0 || L.count == 0) return fail(r, KVRING_ESTATE, "refresh before any write to this layer");
+    if (!r->host_only) {
+        const int H = c.num_heads, d = c.head_dim;
+        const size_t win = (size_t)H * r->Rpad * d, am = (size_t)H * r->Rpad;
+        const size_t buf = (size_t)L.cur * c.num_layers + layer;
+        NaiveRefreshParams p{};
+        p.kw = r->kwin + buf * win;
+        p.vw = r->vwin + buf * win;
+        p.ka = r->kaw + buf * am;
+        p.va = r->vaw + buf * am;
+        p.k8 = r->k8 + (size_t)layer * win;
+        p.vt8 = r->vt8 + (size_t)layer * win;
+        p.kamax = r->kamax + (size_t)layer * am;
+        p.vamax = r->vamax + (size_t)layer * am;
+        p.rope = r->rope;
+        p.pos0 = L.next_pos - L.count;
+        p.count = (int)L.count;
+        p.H = H;
+        p.d = d;
+        p.Rpad = (int)r->Rpad;
+        cudaError_t e = launch_naive_refresh(p, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(r, e, "naive refresh kernel launch");
+        r->launches += 1;
+    }
+    L.fresh = true;
     return KVRING_OK;
 }
 

@@ -38,7 +38,44 @@ struct WriteParams {
     float* part;              // per-block amax partials [K|V][amax_blocks][H] (ring scratch)
 };
 cudaError_t launch_write(const WriteParams& p, cudaStream_t s);   // two launches
+cudaError_t launch_write_amax(const WriteParams& p, cudaStream_t s);   // the first of them alone
 int write_amax_tokens_per_block(int H, int d);
+
+// ---------------------------------------------------------------- naive upkeep (comparison)
+struct NaiveAppendParams {
+    const uint16_t* k;        // new chunk bf16 [T][H][d]
+    const uint16_t* v;
+    const uint16_t* kw_src;   // window before the call, bf16 [H][Rpad][d], logical row order
+    const uint16_t* vw_src;
+    uint16_t* kw_dst;         // window after the call (the other buffer, or the same for a rewrite)
+    uint16_t* vw_dst;
+    const float* ka_src;      // chunk amax of each window row [H][Rpad]
+    const float* va_src;
+    float* ka_dst;
+    float* va_dst;
+    const float* part;        // amax partials of the chunk [K|V][amax_blocks][H]
+    int amax_blocks;
+    int T, H, d, Rpad;
+    int keep;                 // rows kept: dst row r < keep is src row r + drop
+    int drop;                 // oldest rows dropped
+    int row_begin;            // first dst row written (rows below it are already in place)
+};
+cudaError_t launch_naive_append(const NaiveAppendParams& p, cudaStream_t s);
+
+struct NaiveRefreshParams {
+    const uint16_t* kw;       // window bf16 [H][Rpad][d]
+    const uint16_t* vw;
+    const float* ka;          // chunk amax of each row [H][Rpad]
+    const float* va;
+    uint8_t* k8;              // this layer's FP8 cache, as for the write-time ring
+    uint8_t* vt8;
+    float* kamax;
+    float* vamax;
+    const float2* rope;       // [max_position][d/2]
+    int64_t pos0;             // position of row 0
+    int count, H, d, Rpad;
+};
+cudaError_t launch_naive_refresh(const NaiveRefreshParams& p, cudaStream_t s);
 
 // ---------------------------------------------------------------- rebase (K2)
 struct RebaseParams {

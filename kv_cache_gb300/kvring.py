@@ -28,6 +28,7 @@ KVRING_ESTATE = -4
 KVRING_ETIMEOUT = -5
 KVRING_ENODEV = -6
 KVRING_FLAG_HOST_ONLY = 0x1
+KVRING_FLAG_NAIVE_UPKEEP = 0x2
 KVRING_MAX_LAYERS = 256
 
 ERROR_NAMES = {0: "OK", -1: "EINVAL", -2: "ENOMEM", -3: "ECUDA", -4: "ESTATE", -5: "ETIMEOUT", -6: "ENODEV"}
@@ -78,6 +79,7 @@ _SIGNATURES = {
     "kvring_write_ex": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P, ctypes.c_int32, ctypes.c_uint32, _P]),
     "kvring_attend": (ctypes.c_int, [_P, ctypes.c_int32, _P, ctypes.c_int32, _P, _P]),
     "kvring_rebase": (ctypes.c_int, [_P, _P]),
+    "kvring_naive_refresh": (ctypes.c_int, [_P, ctypes.c_int32, _P]),
     "kvring_get_state": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.POINTER(kvring_state)]),
     "kvring_snapshot": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P]),
     "kvring_check_device": (ctypes.c_int, [_P, _P]),
@@ -169,6 +171,10 @@ def kvring_attend(ring, layer: int, q, n_q: int, out, H: int, d: int, stream=Non
     _check(load().kvring_attend(ring, layer, qp, n_q, out.data_ptr(), _stream(stream)), ring)
 
 
+def kvring_naive_refresh(ring, layer: int, stream=None, host_only: bool = False) -> None:
+    _check(load().kvring_naive_refresh(ring, layer, 0 if host_only else _stream(stream)), ring)
+
+
 def kvring_rebase(ring, stream=None, host_only: bool = False) -> None:
     _check(load().kvring_rebase(ring, 0 if host_only else _stream(stream)), ring)
 
@@ -246,9 +252,10 @@ class KVRing:
 
     def __init__(self, num_layers: int, num_heads: int, head_dim: int, capacity: int,
                  max_tokens_per_write: int, max_position: int = 0, rope_theta: float = 10000.0,
-                 host_only: bool = False):
+                 host_only: bool = False, naive_upkeep: bool = False):
+        flags = (KVRING_FLAG_HOST_ONLY if host_only else 0) | (KVRING_FLAG_NAIVE_UPKEEP if naive_upkeep else 0)
         self.cfg = kvring_config(num_layers, num_heads, head_dim, capacity, max_tokens_per_write,
-                                 max_position, rope_theta, KVRING_FLAG_HOST_ONLY if host_only else 0)
+                                 max_position, rope_theta, flags)
         self.L, self.H, self.d, self.R = num_layers, num_heads, head_dim, capacity
         self.host_only = host_only
         self.handle = kvring_create(self.cfg)
@@ -288,6 +295,10 @@ class KVRing:
 
     def rebase(self, stream=None) -> None:
         kvring_rebase(self.handle, stream, host_only=self.host_only)
+
+    def naive_refresh(self, layer: int, stream=None) -> None:
+        """Naive-upkeep rings: re-rotate and re-quantise the layer's whole window."""
+        kvring_naive_refresh(self.handle, layer, stream, host_only=self.host_only)
 
     def state(self, layer: int) -> dict:
         return kvring_get_state(self.handle, layer)

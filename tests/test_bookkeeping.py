@@ -158,3 +158,50 @@ def test_rewrite_errors_leave_state_unchanged():
     assert ring.state(0)["next_pos"] == 180 and ring.state(0)["last_write_pos"] == 160
     assert lib.kvring_write_ex(ring.handle, 0, None, None, 21, 0, None) == kv.KVRING_ESTATE   # 201 > 200
     assert lib.kvring_write_ex(None, 0, None, None, 1, 1, None) == kv.KVRING_EINVAL
+
+
+def _compare_naive(ring, layer, o):
+    st = ring.state(layer)
+    assert (st["count"], st["next_pos"], st["writes"]) == (o.count, o.next_pos, o.writes)
+    assert (st["last_write_pos"], st["last_write_tokens"]) == (o.last_pos, o.last_n)
+    snap = ring.snapshot(layer, cache=False)
+    assert np.array_equal(snap["pos"][:o.count].astype(np.int64), o.pos)
+    assert np.array_equal(snap["chunk"][:o.count].astype(np.int64), o.chunk)
+
+
+@pytest.mark.parametrize("R,T", [(96, 32), (100, 32), (5788, 757), (7, 3)])
+def test_naive_ring_rows_match_the_shifted_window(R, T):
+    # a naive-upkeep ring keeps its rows in logical order: positions and chunk ids
+    # equal the oracle's shifted window through writes, rewrites and resets
+    from oracle.schemes import NaiveWindow
+    ring = kv.KVRing(1, 1, 64, R, T, max_position=R + 42 * T, host_only=True, naive_upkeep=True)
+    o = NaiveWindow(R, 1, 2)
+    z = np.zeros((T, 1, 2), np.float32)
+    for s in range(90):
+        if s > 0 and s % 42 == 0:
+            ring.rebase()
+            o.rebase()
+            _compare_naive(ring, 0, o)
+        ring.write(0, None, None, n_tokens=T)
+        o.write(z, z)
+        _compare_naive(ring, 0, o)
+        if s % 5 == 0:
+            ring.rewrite(0, None, None, n_tokens=T)
+            o.rewrite(z, z)
+            _compare_naive(ring, 0, o)
+        ring.naive_refresh(0)
+
+
+def test_naive_refresh_errors():
+    ring = kv.KVRing(1, 1, 64, 16, 8, host_only=True, naive_upkeep=True)
+    with pytest.raises(kv.KVRingError) as e:
+        ring.naive_refresh(0)
+    assert e.value.code == kv.KVRING_ESTATE
+    with pytest.raises(kv.KVRingError) as e:
+        ring.naive_refresh(1)
+    assert e.value.code == kv.KVRING_EINVAL
+    plain = kv.KVRing(1, 1, 64, 16, 8, host_only=True)
+    plain.write(0, None, None, n_tokens=8)
+    with pytest.raises(kv.KVRingError) as e:
+        plain.naive_refresh(0)
+    assert e.value.code == kv.KVRING_EINVAL and "naive" in e.value.message

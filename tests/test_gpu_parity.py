@@ -205,6 +205,74 @@ def test_rewrite_after_reset_production_sampled():
     assert fk == 1.0 and fv == 1.0
 
 
+def _check_naive(ring, layer, o, what=""):
+    """FP8 cache of a naive-upkeep ring after a refresh against NaiveWindow.cache_codes()."""
+    snap = ring.snapshot(layer)
+    n = o.count
+    k8, v8, _, _ = o.cache_codes()
+    _, _, _, _, ka, va = o.chunk_scales()
+    assert np.array_equal(snap["pos"][:n].astype(np.int64), o.pos), what
+    assert np.array_equal(snap["kamax"][:, :n], ka.T), what
+    assert np.array_equal(snap["vamax"][:, :n], va.T), what
+    fk = assert_codes_match(snap["k"][:, :n], k8.transpose(1, 0, 2), 0.999, "naive K codes " + what)
+    fv = assert_codes_match(snap["v"][:, :n], v8.transpose(1, 0, 2), 0.999, "naive V codes " + what)
+    assert fk == 1.0 and fv == 1.0
+
+
+@pytest.mark.parametrize("R,T,H,d", [(96, 32, 2, 64), (100, 32, 2, 128), (40, 40, 1, 64), (300, 100, 3, 128)])
+def test_naive_upkeep_small(R, T, H, d):
+    """Naive ring: shift on write, newest rows replaced on rewrite, positions reset;
+    each refresh re-rotates and re-quantises the whole window exactly as the oracle."""
+    from oracle.schemes import NaiveWindow
+    ring = kv.KVRing(1, H, d, R, T, max_position=R + 8 * T, naive_upkeep=True)
+    o = NaiveWindow(R, H, d)
+    for s in range(2 * R // T + 6):
+        if s > 0 and s % 8 == 0:
+            ring.rebase()
+            o.rebase()
+        for p in range(2):
+            i = 900 + 2 * s + p
+            kb, kf = chunk_pair("k", i, T, H, d, True)
+            vb, vf = chunk_pair("v", i, T, H, d, True)
+            if p == 0:
+                ring.write(0, to_dev(kb), to_dev(vb))
+                o.write(kf, vf)
+            else:
+                ring.rewrite(0, to_dev(kb), to_dev(vb))
+                o.rewrite(kf, vf)
+            ring.naive_refresh(0)
+            _check_naive(ring, 0, o, f"step {s} pass {p}")
+            qb, qf = chunk_pair("q", i, T, H, d, True)
+            assert_attention_close(ring.attend(0, to_dev(qb)).cpu().numpy(), o.attend(qf), f"step {s} pass {p}")
+
+
+def test_naive_upkeep_production_sampled():
+    """Production shape, naive ring: full window, a reset, refresh, then sampled attention."""
+    from oracle.schemes import NaiveWindow
+    R, T, H, d = 5788, 757, 16, 128
+    ring = kv.KVRing(1, H, d, R, T, max_position=R + 42 * T, naive_upkeep=True)
+    o = NaiveWindow(R, H, d)
+    for w in range(9):
+        kb, kf = chunk_pair("k", 950 + w, T, H, d, True)
+        vb, vf = chunk_pair("v", 950 + w, T, H, d, True)
+        ring.write(0, to_dev(kb), to_dev(vb))
+        o.write(kf, vf)
+    ring.rebase()
+    assert o.rebase() > 0
+    qb, qf = chunk_pair("q", 960, T, H, d, True)
+    with pytest.raises(kv.KVRingError) as e:
+        ring.attend(0, to_dev(qb))
+    assert e.value.code == kv.KVRING_ESTATE
+    ring.naive_refresh(0)
+    _check_naive(ring, 0, o, "production")
+    out = ring.attend(0, to_dev(qb)).cpu().numpy()
+    rng = np.random.default_rng(13)
+    heads = np.array([1, 8, 14])
+    rows = np.unique(np.concatenate([rng.choice(T, 40, replace=False), [0, 128, 756]]))
+    ref = o.attend(qf)[np.ix_(rows, heads)]
+    assert_attention_close(out[np.ix_(rows, heads)], ref, "naive production")
+
+
 def test_edge_sizes():
     # T = 1, T = R (whole ring in one write), then a write that wraps mid-group
     R, H, d = 40, 1, 64
