@@ -298,6 +298,9 @@ def main():
     ap.add_argument("--impl", default="kvring", choices=["kvring", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--small", action="store_true", help="4 blocks instead of 60 (quick checks)")
+    ap.add_argument("--blocks", type=int, default=0,
+                    help="number of blocks (profiling cases; 8 blocks already keep one layer's ring out of L2 "
+                         "between its visits)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--naive-upkeep", action="store_true",
                     help="the comparison scheme: shift the bf16 window on write, re-rotate and re-quantise "
@@ -306,6 +309,9 @@ def main():
                     help="passes 1..3 rewrite the newest chunk with new K/V (kvring_write_ex, no advance)")
     args = ap.parse_args()
     cfg = dict(SMALL if args.small else WORKLOAD)
+    if args.blocks > 0:
+        cfg["name"] = cfg["name"].replace(f"{cfg['L']} blocks", f"{args.blocks} blocks")
+        cfg["L"] = args.blocks
     cfg["writes_per_step"] = cfg["passes"] if args.rewrite_per_pass else 1
     cfg["naive_upkeep"] = bool(args.naive_upkeep)
     if args.rewrite_per_pass:

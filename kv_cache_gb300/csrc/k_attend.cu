@@ -432,6 +432,31 @@ __device__ __forceinline__ float p_group(const uint32_t (&r)[32], const GroupSca
     return lsum;
 }
 
+// The general paths (a group that is not one range) are rare -- a chunk boundary
+// or the ring's last valid slot falls inside the group -- and large once unrolled,
+// so each has one out-of-line copy that reloads the group's 32 scores from tensor
+// memory itself: the hot loop stays small in the instruction cache and no
+// register array crosses the call.
+__device__ __noinline__ float zmax_general(uint32_t taddr, const GroupInfo* info, const float* am, int g, int slot0,
+                                           int count, float a, int lane) {
+    uint32_t r[32];
+    tmem_ld32_async(taddr, r);
+    tmem_wait_ld_dep(r);
+    return zmax_group(r, group_scales(info, am, g, slot0, count, a, lane), a);
+}
+
+// P of group g read from tsrc, stored as 16 packed fp16 columns at tdst; returns
+// the group's share of the row sum.
+__device__ __noinline__ float p_general(uint32_t tsrc, uint32_t tdst, const GroupInfo* info, const float* am, int g,
+                                        int slot0, int count, float a, float M, int lane) {
+    uint32_t r[32], pk[16];
+    tmem_ld32_async(tsrc, r);
+    tmem_wait_ld_dep(r);
+    const float l = p_group(r, group_scales(info, am, g, slot0, count, a, lane), M, a, pk);
+    tmem_st16(tdst, pk);
+    return l;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kAttendThreads, 1)
 attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ AttendMaps maps) {
@@ -556,13 +581,15 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
             uni[1] = (kinds >> 16) == 0;
             return true;
         };
-        // row max of z over two groups (g0, g0 + 1) held in registers
+        // row max of z over two one-range groups (2 hb, 2 hb + 1) held in registers
         auto zmax2 = [&](const uint32_t (&ra)[32], const uint32_t (&rb)[32], int hb) -> float {
-            if (uni[hb])
-                return fmaxf(fmaf(max32(ra), hb ? gk[2] : gk[0], hb ? gl[2] : gl[0]),
-                             fmaf(max32(rb), hb ? gk[3] : gk[1], hb ? gl[3] : gl[1]));
-            return fmaxf(zmax_group(ra, group_scales(info, am, 2 * hb, slot0, p.count, a, lane), a),
-                         zmax_group(rb, group_scales(info, am, 2 * hb + 1, slot0, p.count, a, lane), a));
+            return fmaxf(fmaf(max32(ra), hb ? gk[2] : gk[0], hb ? gl[2] : gl[0]),
+                         fmaf(max32(rb), hb ? gk[3] : gk[1], hb ? gl[3] : gl[1]));
+        };
+        // the same for any groups, read again from tensor memory at taddr (half hb)
+        auto zmax2_general = [&](uint32_t taddr, int hb) -> float {
+            return fmaxf(zmax_general(taddr, info, am, 2 * hb, slot0, p.count, a, lane),
+                         zmax_general(taddr + 32, info, am, 2 * hb + 1, slot0, p.count, a, lane));
         };
         // First pass, one full tile at a time in S buffer j % 2 (S_q or, while it is
         // unused, O_q's columns): the row max M of z.
@@ -579,7 +606,7 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                 tmem_ld32_async(tSj + 32, rb);
                 tmem_wait_ld_dep(ra);
                 tmem_dep(rb);
-                tz = zmax2(ra, rb, 0);
+                tz = uni[0] ? zmax2(ra, rb, 0) : zmax2_general(tSj, 0);
             }
             {
                 uint32_t ra[32], rb[32];
@@ -587,11 +614,18 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                 tmem_ld32_async(tSj + 96, rb);
                 tmem_wait_ld_dep(ra);
                 tmem_dep(rb);
-                // the buffer is free again once read
-                tc_fence_before();
-                __syncwarp();
-                mbar_arrive_warp(&bars[kBPF1 + 2 * q + b]);
-                tz = fmaxf(tz, zmax2(ra, rb, 1));
+                // the buffer is free again once read (the general path reads it again)
+                if (uni[1]) {
+                    tc_fence_before();
+                    __syncwarp();
+                    mbar_arrive_warp(&bars[kBPF1 + 2 * q + b]);
+                    tz = fmaxf(tz, zmax2(ra, rb, 1));
+                } else {
+                    tz = fmaxf(tz, zmax2_general(tSj + 64, 1));
+                    tc_fence_before();
+                    __syncwarp();
+                    mbar_arrive_warp(&bars[kBPF1 + 2 * q + b]);
+                }
             }
             M = fmaxf(M, tz);
             // the end of the stage: its S MMAs are done and its scale rows read
@@ -622,20 +656,18 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                 // (the row's dominant weight is always one of them; the other
                 // elements' rounding is at most 2^-12 of their own, non-dominant,
                 // share); the other kinds sum the rounded values.
-                uint32_t pk[16];
                 float lsum;
                 if (un) {
+                    uint32_t pk[16];
                     lsum = p_one_range(ra, hb ? gk[2] : gk[0], (hb ? gl[2] : gl[0]) - M, max32(ra), hb ? gi[2] : gi[0], pk);
-                } else {
-                    lsum = p_group(ra, group_scales(info, am, g0, slot0, p.count, a, lane), M, a, pk);
-                }
-                tmem_st16(tSb, pk);
-                if (un) {
+                    tmem_st16(tSb, pk);
                     lsum += p_one_range(rb, hb ? gk[3] : gk[1], (hb ? gl[3] : gl[1]) - M, max32(rb), hb ? gi[3] : gi[1], pk);
+                    tmem_st16(tSb + 16, pk);
                 } else {
-                    lsum += p_group(rb, group_scales(info, am, g0 + 1, slot0, p.count, a, lane), M, a, pk);
+                    // group g0's P goes to columns [0, 16) before group g0 + 1 reads [32, 64)
+                    lsum = p_general(tSb, tSb, info, am, g0, slot0, p.count, a, M, lane);
+                    lsum += p_general(tSb + 32, tSb + 16, info, am, g0 + 1, slot0, p.count, a, M, lane);
                 }
-                tmem_st16(tSb + 16, pk);
                 l_run += lsum;
                 // P_q(u) handed over once all 32 lanes' stores are done: one arrival per warp
                 tmem_wait_st();
