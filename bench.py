@@ -282,6 +282,22 @@ def oracle_sample(cfg, seconds_hint=20.0):
                        f"at {H} heads x {d}, R={R}, T={T}; x{L} blocks (extrapolated)")
 
 
+# DRAM bytes (read + write) per attend_kernel launch, from the ncu capture summarised
+# in profiles/attend_kernel_production_ring_8_blocks.md; valid only for the attention
+# source it was taken on (sha256 prefix), else reported as null.
+ATTEND_TRAFFIC = {"bytes": 27.05e6, "source_sha256": "f0d027049025621d"}
+
+
+def attend_traffic():
+    import hashlib
+    path = os.path.join(ROOT, "kv_cache_gb300", "csrc", "k_attend.cu")
+    try:
+        digest = hashlib.sha256(open(path, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return ATTEND_TRAFFIC["bytes"] if digest.startswith(ATTEND_TRAFFIC["source_sha256"]) else None
+
+
 def algorithmic(cfg):
     L, H, d, R, T, P = (cfg[k] for k in ("L", "H", "d", "R", "T", "passes"))
     write_bytes = T * H * d * 2 * 2 + T * H * d * 2           # bf16 K,V in + e4m3 K,V out
@@ -376,7 +392,8 @@ def main():
                 "d2h_bytes_per_step": r["d2h"], "steps": r["e2e_steps"]},
         "gpu_launches": r["launches"],
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": fp8_sustained, "unit": "TFLOP/s",
-                     "frac": attn_tflops / fp8_sustained, "traffic": None,
+                     "frac": attn_tflops / fp8_sustained, "traffic": attend_traffic(),
+                     "traffic_unit": "bytes per attend_kernel launch (ncu, 8-block run)",
                      "kernel": "attention call (q-prep + attention + split combine)",
                      "peak_source": f"{peak_src}: 2 x bf16_tflops_sustained (FP8 = 2 x bf16 nominal ratio)"},
         "breakdown": {
