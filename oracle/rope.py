@@ -1,4 +1,4 @@
-"""1-D rotary position embedding (RoPE).  Test infrastructure.
+"""Rotary position embedding (RoPE), 1-D and 3-D video layouts.  Test infrastructure.
 
 The pages say RoPE is applied to K once, when a chunk is written, and that at
 each position reset one delta rotation is applied to the cached window
@@ -16,6 +16,16 @@ each position reset one delta rotation is applied to the cached window
   separately (no fused multiply-add):
       y0 = x0*c - x1*s
       y1 = x0*s + x1*c
+
+3-D video layout (optional, ``layout=(S, W, pairs_t, pairs_h)``).  The pages do
+not say how the video model lays out its positions; the plain reading for a
+(time, height, width) token grid: a token's running index p = frame * S + s
+(S tokens per frame, W per row) has coordinates t = p // S, h = (p % S) // W,
+w = (p % S) % W.  The d/2 pairs split into three bands -- pairs [0, pairs_t)
+rotate by t, the next pairs_h by h, the rest by w -- each band with its own
+frequencies theta ** (-2k / d_band), k < d_band / 2, d_band = 2 * pairs in the
+band.  A shift by whole frames changes only t, so a position reset rotates only
+the temporal band.
 """
 from __future__ import annotations
 
@@ -31,23 +41,42 @@ def freqs(d: int, theta: float = 10000.0) -> list:
     return [math.pow(float(theta), -2.0 * i / d) for i in range(d // 2)]
 
 
-def angle_table(positions, d: int, theta: float = 10000.0):
+def coords_3d(p: int, S: int, W: int):
+    """(t, h, w) of running token index p in frames of S tokens, W per row."""
+    t, s = divmod(int(p), S)
+    return t, s // W, s % W
+
+
+def pair_angles(p: int, d: int, theta: float = 10000.0, layout=None) -> list:
+    """float64 angle of each of the d/2 pairs for running position p."""
+    if layout is None:
+        return [float(p) * wi for wi in freqs(d, theta)]
+    S, W, pt, ph = layout
+    pw = d // 2 - pt - ph
+    t, h, w = coords_3d(p, S, W)
+    ang = [float(t) * wi for wi in freqs(2 * pt, theta)]
+    ang += [float(h) * wi for wi in freqs(2 * ph, theta)]
+    ang += [float(w) * wi for wi in freqs(2 * pw, theta)]
+    return ang
+
+
+def angle_table(positions, d: int, theta: float = 10000.0, layout=None):
     """(cos, sin) float32 arrays of shape [len(positions), d/2].
 
-    Entry [n, i] is fp32(cos(p_n * w_i)) / fp32(sin(p_n * w_i)), the angle
-    formed and evaluated in float64.  Negative positions are allowed (the
-    delta rotation of a reset uses -delta).
+    Entry [n, i] is fp32(cos(a)) / fp32(sin(a)) of pair i's angle a at position
+    p_n (1-D: p_n * w_i; 3-D: the band's coordinate times its frequency), formed
+    and evaluated in float64.  Negative positions are allowed (the delta
+    rotation of a reset uses -delta).
     """
     positions = [int(p) for p in np.asarray(positions).reshape(-1)]
-    w = freqs(d, theta)
-    key = (d, float(theta))
+    key = (d, float(theta), layout)
     cache = _TABLE_CACHE.setdefault(key, {})
     c = np.empty((len(positions), d // 2), dtype=np.float32)
     s = np.empty((len(positions), d // 2), dtype=np.float32)
     for n, p in enumerate(positions):
         row = cache.get(p)
         if row is None:
-            ang = [float(p) * wi for wi in w]
+            ang = pair_angles(p, d, theta, layout)
             row = (np.array([math.cos(a) for a in ang], dtype=np.float32),
                    np.array([math.sin(a) for a in ang], dtype=np.float32))
             cache[p] = row
@@ -76,9 +105,9 @@ def rotate(x: np.ndarray, cos: np.ndarray, sin: np.ndarray) -> np.ndarray:
     return y
 
 
-def rotate_at(x: np.ndarray, positions, d: int, theta: float = 10000.0) -> np.ndarray:
+def rotate_at(x: np.ndarray, positions, d: int, theta: float = 10000.0, layout=None) -> np.ndarray:
     """Rotate rows x[n, ..., d] by position positions[n]."""
-    c, s = angle_table(positions, d, theta)
+    c, s = angle_table(positions, d, theta, layout)
     extra = x.ndim - 2
     shape = (c.shape[0],) + (1,) * extra + (c.shape[1],)
     return rotate(x, c.reshape(shape), s.reshape(shape))

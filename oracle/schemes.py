@@ -96,20 +96,20 @@ def dequantise_f64(code: np.ndarray, scale: np.ndarray) -> np.ndarray:
     return e4m3.decode(code) * np.asarray(scale, dtype=np.float64)
 
 
-def quantise_q(q: np.ndarray, positions, d: int, theta: float):
+def quantise_q(q: np.ndarray, positions, d: int, theta: float, layout=None):
     """Rotate q [T][H][d] at positions[T] and quantise each (token, head) row.
 
     Returns (codes uint8 [T][H][d], amax float32 [T][H]).
     """
-    qr = rope.rotate_at(np.asarray(q, dtype=F32), positions, d, theta)
+    qr = rope.rotate_at(np.asarray(q, dtype=F32), positions, d, theta, layout)
     amax = np.abs(qr).max(axis=2).astype(F32) if qr.shape[0] else np.zeros(qr.shape[:2], F32)
     _, inv = scale_inv(amax)
     codes = quantise(qr, inv[..., None])
     return codes, amax
 
 
-def dequantised_q(q: np.ndarray, positions, d: int, theta: float) -> np.ndarray:
-    codes, amax = quantise_q(q, positions, d, theta)
+def dequantised_q(q: np.ndarray, positions, d: int, theta: float, layout=None) -> np.ndarray:
+    codes, amax = quantise_q(q, positions, d, theta, layout)
     scale, _ = scale_inv(amax)
     return dequantise_f64(codes, scale[..., None])
 
@@ -117,8 +117,9 @@ def dequantised_q(q: np.ndarray, positions, d: int, theta: float) -> np.ndarray:
 class NaiveWindow:
     """Shift-the-window cache that redoes RoPE and quantisation on every call."""
 
-    def __init__(self, capacity: int, num_heads: int, head_dim: int, theta: float = 10000.0):
+    def __init__(self, capacity: int, num_heads: int, head_dim: int, theta: float = 10000.0, layout=None):
         self.R, self.H, self.d, self.theta = capacity, num_heads, head_dim, float(theta)
+        self.layout = layout
         self.k = np.zeros((0, num_heads, head_dim), F32)   # un-rotated bf16 values
         self.v = np.zeros((0, num_heads, head_dim), F32)
         self.pos = np.zeros(0, np.int64)
@@ -191,7 +192,7 @@ class NaiveWindow:
         Returns (k codes, v codes, kscale, vscale) in logical order.
         """
         ks, ki, vs, vi, _, _ = self.chunk_scales()
-        kr = rope.rotate_at(self.k, self.pos, self.d, self.theta)
+        kr = rope.rotate_at(self.k, self.pos, self.d, self.theta, self.layout)
         k8 = quantise(kr, ki[..., None])
         v8 = quantise(self.v, vi[..., None])
         return k8, v8, ks, vs
@@ -202,16 +203,17 @@ class NaiveWindow:
         kd = dequantise_f64(k8, ks[..., None])
         vd = dequantise_f64(v8, vs[..., None])
         qpos = self.last_pos + np.arange(q.shape[0], dtype=np.int64)
-        qd = dequantised_q(q, qpos, self.d, self.theta)
+        qd = dequantised_q(q, qpos, self.d, self.theta, self.layout)
         return attention_fp64(qd, kd, vd)
 
 
 class WriteTimeRing:
     """Ring-buffer cache: RoPE and FP8 once at write, delta rotation at reset."""
 
-    def __init__(self, capacity: int, num_heads: int, head_dim: int, theta: float = 10000.0):
+    def __init__(self, capacity: int, num_heads: int, head_dim: int, theta: float = 10000.0, layout=None):
         R, H, d = capacity, num_heads, head_dim
         self.R, self.H, self.d, self.theta = R, H, d, float(theta)
+        self.layout = layout
         self.k8 = np.zeros((H, R, d), np.uint8)
         self.v8 = np.zeros((H, R, d), np.uint8)
         self.kamax = np.zeros((H, R), F32)
@@ -267,7 +269,7 @@ class WriteTimeRing:
         va = chunk_amax_v(v)
         _, ki = scale_inv(ka)
         _, vi = scale_inv(va)
-        kr = rope.rotate_at(k, pos, self.d, self.theta)           # [T][H][d]
+        kr = rope.rotate_at(k, pos, self.d, self.theta, self.layout)   # [T][H][d]
         k8 = quantise(kr, ki[None, :, None])
         v8 = quantise(v, vi[None, :, None])
         self.k8[:, slots, :] = k8.transpose(1, 0, 2)
@@ -282,7 +284,7 @@ class WriteTimeRing:
         delta = self.next_pos - self.count
         if delta != 0 and self.count > 0:
             valid = np.nonzero(self.pos >= 0)[0]
-            c, s = rope.angle_table([-delta], self.d, self.theta)    # [1][d/2]
+            c, s = rope.angle_table([-delta], self.d, self.theta, self.layout)   # [1][d/2]
             ks, ki = scale_inv(self.kamax[:, valid])                 # [H][n]
             x = dequantise_f32(self.k8[:, valid, :], ks[..., None])
             xr = rope.rotate(x, c[0], s[0])
@@ -311,5 +313,5 @@ class WriteTimeRing:
         kd = dequantise_f64(self.k8[np.ix_(heads, valid)], ks[..., None]).transpose(1, 0, 2)
         vd = dequantise_f64(self.v8[np.ix_(heads, valid)], vs[..., None]).transpose(1, 0, 2)
         qpos = self.last_pos + rows.astype(np.int64)
-        qd = dequantised_q(np.asarray(q, F32)[np.ix_(rows, heads)], qpos, self.d, self.theta)
+        qd = dequantised_q(np.asarray(q, F32)[np.ix_(rows, heads)], qpos, self.d, self.theta, self.layout)
         return attention_fp64(qd, kd, vd)

@@ -116,6 +116,25 @@ class _RewriteStaleScale(schemes_mod.WriteTimeRing):
         return slots
 
 
+def _coords_swapped(p, S, W):
+    t, s = divmod(int(p), S)
+    return t, s % W, s // W
+
+
+def _pair_angles_full_width(p, d, theta=10000.0, layout=None):
+    # every band takes the frequencies of the whole head width
+    if layout is None:
+        return _ORIG_PAIR_ANGLES(p, d, theta, None)
+    S, W, pt, ph = layout
+    t, h, w = rope_mod.coords_3d(p, S, W)
+    f = rope_mod.freqs(d, theta)
+    return [float(t) * f[i] for i in range(pt)] + [float(h) * f[pt + i] for i in range(ph)] + \
+        [float(w) * f[pt + ph + i] for i in range(d // 2 - pt - ph)]
+
+
+_ORIG_PAIR_ANGLES = rope_mod.pair_angles
+
+
 CASES = [
     ("rotation sign", [(rope_mod, "rotate", _rotate_sign_flipped)], t_rope.test_unit_vector_rotates_to_cos_sin),
     ("rotate-half pairing", [(rope_mod, "rotate", _rotate_halves)], t_rope.test_matches_complex_multiplication),
@@ -125,6 +144,8 @@ CASES = [
     ("softmax axis", [(t_att, "attention_fp64", _attention_transposed)], t_att.test_rows_are_convex_combinations_and_key_order_free),
     ("K amax not pair norm", [(t_sch, "chunk_amax_k", _amax_plain)], t_sch.test_amax_k_is_largest_pair_norm_bruteforce),
     ("ring head drift", [(t_ring, "WriteTimeRing", _RingOffByOne)], lambda: t_ring.test_logical_order_equals_shifted_window(96, 32)),
+    ("3-D height/width swapped", [(rope_mod, "coords_3d", _coords_swapped)], t_rope.test_3d_each_band_is_1d_rope_at_its_coordinate),
+    ("3-D band frequencies", [(rope_mod, "pair_angles", _pair_angles_full_width)], t_rope.test_3d_each_band_is_1d_rope_at_its_coordinate),
     ("rewrite slots", [(t_ring, "WriteTimeRing", _RewriteNextSlots)], lambda: t_ring.test_rewrite_equals_writing_that_chunk(10, 4, 3)),
     ("rewrite positions", [(t_ring, "WriteTimeRing", _RewriteNextPositions)], t_ring.test_rewrite_after_reset_uses_the_shifted_positions),
     ("rewrite stale scale", [(t_ring, "WriteTimeRing", _RewriteStaleScale)], lambda: t_ring.test_rewrite_equals_writing_that_chunk(12, 4, 3)),

@@ -183,3 +183,34 @@ def test_rewrite_needs_a_write_of_the_same_size():
     r.write(_zeros(4), _zeros(4))
     with pytest.raises(AssertionError):
         r.rewrite(_zeros(3), _zeros(3))
+
+
+def test_3d_reset_rotates_only_the_time_band():
+    # with the 3-D layout a reset is a whole number of frames: the codes of the
+    # height and width bands stay as they are, the time band turns; the window's
+    # time-band codes agree with a fresh write at the shifted frames within one
+    # pair step (reading of the rebase for 1-D RoPE)
+    from oracle.schemes import NaiveWindow
+    R, T, H, d, S, W = 48, 12, 2, 64, 12, 4
+    lay = (S, W, 12, 10)
+    ring = WriteTimeRing(R, H, d, layout=lay)
+    naive = NaiveWindow(R, H, d, layout=lay)
+    rng = np.random.default_rng(9)
+    for w in range(7):
+        k = rng.standard_normal((T, H, d)).astype(np.float32)
+        v = rng.standard_normal((T, H, d)).astype(np.float32)
+        ring.write(k, v)
+        naive.write(k, v)
+    before = ring.k8.copy()
+    assert ring.rebase() == naive.rebase() == 3 * T
+    assert np.array_equal(ring.k8[..., 24:], before[..., 24:])
+    assert np.mean(ring.k8[..., :24] != before[..., :24]) > 0.3
+    k8, _, _, _ = naive.cache_codes()
+    idx = (ring.head - ring.count + np.arange(ring.count)) % R
+    from oracle import e4m3
+    a = e4m3.decode(ring.k8[:, idx])
+    b = e4m3.decode(k8.transpose(1, 0, 2))
+    big = np.maximum(np.abs(a), np.abs(b))
+    pair_big = np.maximum(big[..., 0::2], big[..., 1::2])
+    step = e4m3.ulp_at(np.repeat(pair_big, 2, axis=-1))
+    assert np.max(np.abs(a - b) / step) <= 1.0

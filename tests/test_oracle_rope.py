@@ -95,3 +95,75 @@ def test_angles_formed_in_float64():
     for i in (0, 1, 5):
         assert c[0, i] == np.float32(math.cos(p * w[i]))
         assert s[0, i] == np.float32(math.sin(p * w[i]))
+
+
+# ---- 3-D video layout: frames of S tokens, W per row; pairs split (t, h, w)
+
+def _layout(d, S, W, pt, ph):
+    assert pt + ph < d // 2
+    return (S, W, pt, ph)
+
+
+def test_3d_one_token_frames_is_1d_rope_on_the_time_band():
+    # S = W = 1: every token is its own frame at h = w = 0, so the time band is the
+    # 1-D RoPE of width 2 pt at the token's index and the other pairs stay exactly
+    d, pt, ph = 64, 12, 10
+    lay = _layout(d, 1, 1, pt, ph)
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal((40, 3, d)).astype(np.float32)
+    pos = rng.integers(0, 30000, size=40)
+    y = rope.rotate_at(x, pos, d, layout=lay)
+    assert np.array_equal(y[..., :2 * pt], rope.rotate_at(x[..., :2 * pt], pos, 2 * pt))
+    assert np.array_equal(y[..., 2 * pt:], x[..., 2 * pt:])
+
+
+def test_3d_each_band_is_1d_rope_at_its_coordinate():
+    # frames of 12 tokens in rows of 4: band h sees the row, band w the column,
+    # band t the frame; each band equals the 1-D RoPE of its width at that index
+    d, S, W, pt, ph = 128, 12, 4, 22, 21
+    pw = d // 2 - pt - ph
+    lay = _layout(d, S, W, pt, ph)
+    rng = np.random.default_rng(2)
+    pos = np.arange(5 * S + 3)
+    x = rng.standard_normal((len(pos), 2, d)).astype(np.float32)
+    y = rope.rotate_at(x, pos, d, layout=lay)
+    t, s = pos // S, pos % S
+    bands = [(0, pt, t), (pt, ph, s // W), (pt + ph, pw, s % W)]
+    for start, n, coord in bands:
+        sl = slice(2 * start, 2 * (start + n))
+        assert np.array_equal(y[..., sl], rope.rotate_at(x[..., sl], coord, 2 * n))
+
+
+def test_3d_frame_shift_composes():
+    # rotating at p and then by -delta frames equals rotating at p - delta (fp32)
+    d, S, W = 128, 12, 4
+    lay = _layout(d, S, W, 22, 21)
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((64, d)).astype(np.float32)
+    pos = rng.integers(6000, 9000, size=64)
+    delta = 250 * S
+    c, s = rope.angle_table([-delta], d, layout=lay)
+    twice = rope.rotate(rope.rotate_at(x, pos, d, layout=lay), c[0], s[0])
+    once = rope.rotate_at(x, pos - delta, d, layout=lay)
+    assert np.max(np.abs(twice - once)) < 1e-5 * max(1.0, np.max(np.abs(x)))
+    # the reset's rotation row turns the height and width bands by exactly zero
+    assert np.all(c[0, 22:] == 1.0) and np.all(s[0, 22:] == 0.0)
+
+
+def test_3d_scores_depend_on_coordinate_differences_only():
+    # q.k after rotation is unchanged when both tokens move by the same number of
+    # frames (relative-position property of each band)
+    d, S, W = 64, 20, 5
+    lay = _layout(d, S, W, 12, 10)
+    rng = np.random.default_rng(4)
+    q = rng.standard_normal((30, d)).astype(np.float64)
+    k = rng.standard_normal((30, d)).astype(np.float64)
+    pq = rng.integers(0, 400, size=30)
+    pk = rng.integers(0, 400, size=30)
+    def score(shift):
+        rq = rope.rotate_at(q.astype(np.float32), pq + shift, d, layout=lay).astype(np.float64)
+        rk = rope.rotate_at(k.astype(np.float32), pk + shift, d, layout=lay).astype(np.float64)
+        return np.sum(rq * rk, axis=-1)
+    assert np.max(np.abs(score(0) - score(37 * S))) < 1e-4
+    # a shift that is not a whole number of frames moves the spatial coordinates
+    assert np.max(np.abs(score(0) - score(3))) > 1e-2
