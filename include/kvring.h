@@ -66,6 +66,19 @@ extern "C" {
  * cache equals a fresh rotation at the current positions.  Uses 4 bytes per
  * element more device memory than a write-time ring (two bf16 window copies). */
 #define KVRING_FLAG_NAIVE_UPKEEP 0x2u
+/* 3-D (time, height, width) video RoPE.  The pages do not give the layout; the
+ * plain reading for a video token grid: a token's running index p (the position
+ * the ring counts) is frame * S + s with S = frame_tokens tokens per frame and
+ * frame_width tokens per row, so its coordinates are t = p / S,
+ * h = (p % S) / frame_width, w = (p % S) % frame_width.  Pairs [0, pt) rotate by
+ * t, the next ph pairs by h and the remaining pw = d/2 - pt - ph by w, each band
+ * with its own frequencies theta^(-2k/d_band), d_band = 2 x its pairs.  Every
+ * write is a whole number of frames (n_tokens % S == 0) and capacity % S == 0,
+ * so a position reset moves whole frames: it turns only the time band, and
+ * kvring_rebase reads and writes only the 16-byte pieces of K that hold time
+ * pairs (ceil(pt / 8) of the d/16 pieces per row); every other pair keeps its
+ * codes exactly. */
+#define KVRING_FLAG_ROPE_3D 0x4u
 
 #define KVRING_MAX_LAYERS 256
 
@@ -81,6 +94,11 @@ typedef struct {
                                         size of the RoPE table (max_position x d/2 x 8 bytes) */
     float    rope_theta;             /* RoPE base; 0 -> 10000                                */
     uint32_t flags;                  /* KVRING_FLAG_*                                        */
+    /* KVRING_FLAG_ROPE_3D only (ignored otherwise): */
+    int32_t  frame_tokens;           /* S: tokens per frame, >= 1, divides capacity          */
+    int32_t  frame_width;            /* tokens per row of a frame, >= 1, divides S           */
+    int32_t  rope_pairs_t;           /* pt: pairs of the time band; 0 -> d/2 - 2*floor(d/6)  */
+    int32_t  rope_pairs_h;           /* ph: pairs of the height band; 0 -> floor(d/6)        */
 } kvring_config;
 
 typedef struct {
@@ -115,7 +133,8 @@ int kvring_destroy(kvring_t* ring);
  * each of its slots and never changes.
  * Then head += n (mod R), count = min(count + n, R), next_pos += n.
  * n_tokens == 0 is a no-op.  Errors: EINVAL (layer, pointers, n_tokens >
- * max_tokens_per_write), ESTATE (next_pos + n_tokens > max_position), ECUDA. */
+ * max_tokens_per_write, or not a whole number of frames on a 3-D ring), ESTATE
+ * (next_pos + n_tokens > max_position), ECUDA. */
 int kvring_write(kvring_t* ring, int32_t layer, const void* k_bf16, const void* v_bf16,
                  int32_t n_tokens, void* cuda_stream);
 

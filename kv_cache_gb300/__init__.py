@@ -8,4 +8,4 @@ from .kvring import (KVRING_EINVAL, KVRING_ENODEV, KVRING_ENOMEM, KVRING_ECUDA, 
                      KVRING_ETIMEOUT, KVRING_OK, KVRing, KVRingError, kvring_attend, kvring_attend_noalloc, kvring_check_device,
                      kvring_config, kvring_create, kvring_debug_fault, kvring_destroy, kvring_get_state,
                      kvring_last_error, kvring_launch_count, kvring_rebase, kvring_snapshot, kvring_state, kvring_write,
-                     kvring_write_ex, KVRING_WRITE_REWRITE, KVRING_FLAG_NAIVE_UPKEEP, kvring_naive_refresh)
+                     kvring_write_ex, KVRING_WRITE_REWRITE, KVRING_FLAG_NAIVE_UPKEEP, kvring_naive_refresh, KVRING_FLAG_ROPE_3D)

@@ -40,6 +40,7 @@ struct kvring {
     kvring_config cfg{};
     bool host_only = false;
     bool naive = false;         // KVRING_FLAG_NAIVE_UPKEEP
+    bool rope3d = false;        // KVRING_FLAG_ROPE_3D
     int device = 0, num_sms = 0;
     int64_t Rpad = 0, Tstride = 0;
     int max_splits = 1;
@@ -98,10 +99,28 @@ void free_device(kvring_t* r) {
 
 // Angles p * w_i formed and evaluated in float64 (w_i = theta^(-2i/d)), cos and
 // sin rounded once to float32; one row of d/2 (cos, sin) pairs per position.
-void build_rope_table(std::vector<float2>& tab, int max_pos, int d, double theta) {
+// 3-D video layout (KVRING_FLAG_ROPE_3D): running index p = frame * S + s has
+// coordinates t = p / S, h = s / W, w = s % W; pairs [0, pt) turn by t, the next
+// ph by h, the rest by w, each band with the frequencies of its own width.
+struct Rope3D {
+    int S, W, pt, ph;
+};
+
+void build_rope_table(std::vector<float2>& tab, int max_pos, int d, double theta, const Rope3D* r3) {
     const int half = d / 2;
     std::vector<double> w(half);
-    for (int i = 0; i < half; ++i) w[i] = std::pow(theta, -2.0 * i / d);
+    std::vector<int> band(half, 0);   // 3-D: 0 = time, 1 = height, 2 = width
+    if (!r3) {
+        for (int i = 0; i < half; ++i) w[i] = std::pow(theta, -2.0 * i / d);
+    } else {
+        const int n[3] = {r3->pt, r3->ph, half - r3->pt - r3->ph};
+        int i = 0;
+        for (int b = 0; b < 3; ++b)
+            for (int k = 0; k < n[b]; ++k, ++i) {
+                w[i] = std::pow(theta, -2.0 * k / (2 * n[b]));
+                band[i] = b;
+            }
+    }
     tab.resize((size_t)max_pos * half);
     unsigned nth = std::max(1u, std::min(16u, std::thread::hardware_concurrency()));
     std::vector<std::thread> th;
@@ -109,7 +128,12 @@ void build_rope_table(std::vector<float2>& tab, int max_pos, int d, double theta
         th.emplace_back([&, k] {
             for (int64_t p = k; p < max_pos; p += nth)
                 for (int i = 0; i < half; ++i) {
-                    const double ang = (double)p * w[i];
+                    int64_t coord = p;
+                    if (r3) {
+                        const int64_t s = p % r3->S;
+                        coord = band[i] == 0 ? p / r3->S : band[i] == 1 ? s / r3->W : s % r3->W;
+                    }
+                    const double ang = (double)coord * w[i];
                     tab[(size_t)p * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
                 }
         });
@@ -146,7 +170,19 @@ int check_config(const kvring_config* c) {
         return fail(nullptr, KVRING_EINVAL, "max_tokens_per_write out of range [1, min(capacity, 2048)]");
     if (c->max_position < 0) return fail(nullptr, KVRING_EINVAL, "max_position must be >= 0");
     if (c->rope_theta < 0 || !std::isfinite(c->rope_theta)) return fail(nullptr, KVRING_EINVAL, "rope_theta must be finite and >= 0");
-    if (c->flags & ~(KVRING_FLAG_HOST_ONLY | KVRING_FLAG_NAIVE_UPKEEP)) return fail(nullptr, KVRING_EINVAL, "unknown flag bits");
+    if (c->flags & ~(KVRING_FLAG_HOST_ONLY | KVRING_FLAG_NAIVE_UPKEEP | KVRING_FLAG_ROPE_3D))
+        return fail(nullptr, KVRING_EINVAL, "unknown flag bits");
+    if (c->flags & KVRING_FLAG_ROPE_3D) {
+        if (c->frame_tokens < 1 || c->frame_width < 1 || c->frame_tokens % c->frame_width != 0)
+            return fail(nullptr, KVRING_EINVAL, "3-D RoPE: frame_tokens and frame_width must be >= 1, frame_width dividing frame_tokens");
+        if (c->capacity % c->frame_tokens != 0)
+            return fail(nullptr, KVRING_EINVAL, "3-D RoPE: capacity must be a whole number of frames");
+        const int half = c->head_dim / 2;
+        if (c->rope_pairs_t != 0 || c->rope_pairs_h != 0) {
+            if (c->rope_pairs_t < 1 || c->rope_pairs_h < 1 || c->rope_pairs_t + c->rope_pairs_h > half - 1)
+                return fail(nullptr, KVRING_EINVAL, "3-D RoPE: each band needs at least one pair (pt + ph <= d/2 - 1)");
+        }
+    }
     return KVRING_OK;
 }
 
@@ -266,6 +302,12 @@ int kvring_create(const kvring_config* cfg_in, kvring_t** out) {
     r->cfg = cfg;
     r->host_only = (cfg.flags & KVRING_FLAG_HOST_ONLY) != 0;
     r->naive = (cfg.flags & KVRING_FLAG_NAIVE_UPKEEP) != 0;
+    r->rope3d = (cfg.flags & KVRING_FLAG_ROPE_3D) != 0;
+    if (r->rope3d && cfg.rope_pairs_t == 0 && cfg.rope_pairs_h == 0) {
+        cfg.rope_pairs_h = cfg.head_dim / 6;
+        cfg.rope_pairs_t = cfg.head_dim / 2 - 2 * cfg.rope_pairs_h;
+        r->cfg = cfg;
+    }
     r->Rpad = round_up(cfg.capacity, 128);
     r->Tstride = round_up(cfg.max_tokens_per_write, 256);
     r->layers.resize(cfg.num_layers);
@@ -325,7 +367,8 @@ int kvring_create(const kvring_config* cfg_in, kvring_t** out) {
     }
     {
         std::vector<float2> tab;
-        build_rope_table(tab, cfg.max_position, (int)d, (double)cfg.rope_theta);
+        const Rope3D r3{cfg.frame_tokens, cfg.frame_width, cfg.rope_pairs_t, cfg.rope_pairs_h};
+        build_rope_table(tab, cfg.max_position, (int)d, (double)cfg.rope_theta, r->rope3d ? &r3 : nullptr);
         e = cudaMemcpy(r->rope, tab.data(), rope_bytes, cudaMemcpyHostToDevice);
         if (e != cudaSuccess) { free_device(r); delete r; return fail(nullptr, KVRING_ECUDA, std::string("cudaMemcpy: ") + cudaGetErrorString(e)); }
     }
@@ -367,6 +410,8 @@ int kvring_write_ex(kvring_t* r, int32_t layer, const void* k, const void* v, in
     if (layer < 0 || layer >= c.num_layers) return fail(r, KVRING_EINVAL, "layer out of range");
     if (flags & ~KVRING_WRITE_REWRITE) return fail(r, KVRING_EINVAL, "unknown write flag");
     if (n < 0 || n > c.max_tokens_per_write) return fail(r, KVRING_EINVAL, "n_tokens out of range [0, max_tokens_per_write]");
+    if (r->rope3d && n % c.frame_tokens != 0)
+        return fail(r, KVRING_EINVAL, "3-D RoPE: n_tokens must be a whole number of frames");
     LayerState& L = r->layers[layer];
     const bool rewrite = (flags & KVRING_WRITE_REWRITE) != 0;
     if (rewrite && L.writes == 0) return fail(r, KVRING_ESTATE, "rewrite before any write to this layer");
@@ -523,6 +568,8 @@ int kvring_rebase(kvring_t* r, void* stream) {
         p.H = c.num_heads;
         p.d = c.head_dim;
         p.Rpad = (int)r->Rpad;
+        // 3-D: a reset moves whole frames and turns only the time pairs
+        p.pairs = r->rope3d ? c.rope_pairs_t : c.head_dim / 2;
         cudaError_t e = launch_rebase(p, r->num_sms, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(r, e, "rebase kernel launch");
         r->launches += 1;

@@ -83,6 +83,7 @@ struct RebaseParams {
     const float* kamax;       // all layers [L][H][Rpad]
     const float2* rope;       // [max_position][d/2]
     int L, H, d, Rpad;
+    int pairs;                      // leading pairs of a row that turn (d/2; the time band for 3-D RoPE)
     int delta[KVRING_MAX_LAYERS];   // per layer; 0 = skip
     int count[KVRING_MAX_LAYERS];   // valid slots per layer
 };

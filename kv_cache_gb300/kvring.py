@@ -29,6 +29,7 @@ KVRING_ETIMEOUT = -5
 KVRING_ENODEV = -6
 KVRING_FLAG_HOST_ONLY = 0x1
 KVRING_FLAG_NAIVE_UPKEEP = 0x2
+KVRING_FLAG_ROPE_3D = 0x4
 KVRING_MAX_LAYERS = 256
 
 ERROR_NAMES = {0: "OK", -1: "EINVAL", -2: "ENOMEM", -3: "ECUDA", -4: "ESTATE", -5: "ETIMEOUT", -6: "ENODEV"}
@@ -44,6 +45,10 @@ class kvring_config(ctypes.Structure):
         ("max_position", ctypes.c_int32),
         ("rope_theta", ctypes.c_float),
         ("flags", ctypes.c_uint32),
+        ("frame_tokens", ctypes.c_int32),
+        ("frame_width", ctypes.c_int32),
+        ("rope_pairs_t", ctypes.c_int32),
+        ("rope_pairs_h", ctypes.c_int32),
     ]
 
 
@@ -252,10 +257,14 @@ class KVRing:
 
     def __init__(self, num_layers: int, num_heads: int, head_dim: int, capacity: int,
                  max_tokens_per_write: int, max_position: int = 0, rope_theta: float = 10000.0,
-                 host_only: bool = False, naive_upkeep: bool = False):
+                 host_only: bool = False, naive_upkeep: bool = False, rope_3d=None):
+        """rope_3d: None (1-D RoPE) or (frame_tokens, frame_width, pairs_t, pairs_h); pairs 0, 0 = default split."""
         flags = (KVRING_FLAG_HOST_ONLY if host_only else 0) | (KVRING_FLAG_NAIVE_UPKEEP if naive_upkeep else 0)
+        S, W, pt, ph = rope_3d if rope_3d is not None else (0, 0, 0, 0)
+        if rope_3d is not None:
+            flags |= KVRING_FLAG_ROPE_3D
         self.cfg = kvring_config(num_layers, num_heads, head_dim, capacity, max_tokens_per_write,
-                                 max_position, rope_theta, flags)
+                                 max_position, rope_theta, flags, S, W, pt, ph)
         self.L, self.H, self.d, self.R = num_layers, num_heads, head_dim, capacity
         self.host_only = host_only
         self.handle = kvring_create(self.cfg)

@@ -285,10 +285,15 @@ class WriteTimeRing:
         if delta != 0 and self.count > 0:
             valid = np.nonzero(self.pos >= 0)[0]
             c, s = rope.angle_table([-delta], self.d, self.theta, self.layout)   # [1][d/2]
+            # pairs the reset turns: all of them in 1-D; in the 3-D layout a reset
+            # moves whole frames and only the time band turns -- the other pairs'
+            # codes stay as stored (a rotation by exactly zero could still flip
+            # the sign of a zero code)
+            n = self.d // 2 if self.layout is None else self.layout[2]
             ks, ki = scale_inv(self.kamax[:, valid])                 # [H][n]
-            x = dequantise_f32(self.k8[:, valid, :], ks[..., None])
-            xr = rope.rotate(x, c[0], s[0])
-            self.k8[:, valid, :] = quantise(xr, ki[..., None])
+            x = dequantise_f32(self.k8[:, valid, :2 * n], ks[..., None])
+            xr = rope.rotate(x, c[0, :n], s[0, :n])
+            self.k8[:, valid, :2 * n] = quantise(xr, ki[..., None])
             self.pos[valid] -= delta
         self.next_pos = self.count
         self.last_pos -= delta

@@ -30,5 +30,5 @@ def test_library_exports_every_declared_symbol():
 
 def test_struct_layouts_match_header():
     ensure_built()
-    assert ctypes.sizeof(kv.kvring_config) == 8 * 4
+    assert ctypes.sizeof(kv.kvring_config) == 12 * 4
     assert ctypes.sizeof(kv.kvring_state) == 7 * 8

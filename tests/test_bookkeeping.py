@@ -100,7 +100,7 @@ def test_attend_needs_a_device_ring():
 
 @pytest.mark.parametrize("field,value", [("num_layers", 0), ("num_layers", 257), ("num_heads", 0),
                                          ("head_dim", 96), ("capacity", 0), ("max_tokens_per_write", 0),
-                                         ("max_tokens_per_write", 97), ("max_position", -1), ("flags", 4)])
+                                         ("max_tokens_per_write", 97), ("max_position", -1), ("flags", 8)])
 def test_create_rejects_bad_config(field, value):
     cfg = kv.kvring_config(1, 2, 64, 96, 32, 0, 10000.0, kv.KVRING_FLAG_HOST_ONLY)
     setattr(cfg, field, value)
@@ -205,3 +205,32 @@ def test_naive_refresh_errors():
     with pytest.raises(kv.KVRingError) as e:
         plain.naive_refresh(0)
     assert e.value.code == kv.KVRING_EINVAL and "naive" in e.value.message
+
+
+@pytest.mark.parametrize("S,W,pt,ph,R", [(0, 1, 0, 0, 96), (12, 5, 0, 0, 96), (12, 4, 0, 0, 100),
+                                          (12, 4, 16, 16, 96), (12, 4, 0, 5, 96), (12, 4, 31, 1, 96)])
+def test_create_rejects_bad_3d_layout(S, W, pt, ph, R):
+    cfg = kv.kvring_config(1, 2, 64, R, 24, 0, 10000.0, kv.KVRING_FLAG_HOST_ONLY | kv.KVRING_FLAG_ROPE_3D,
+                           S, W, pt, ph)
+    with pytest.raises(kv.KVRingError) as e:
+        kv.kvring_create(cfg)
+    assert e.value.code == kv.KVRING_EINVAL and "3-D" in e.value.message
+
+
+def test_3d_ring_writes_whole_frames_and_resets_by_frames():
+    from oracle.schemes import WriteTimeRing
+    S, R, T = 12, 96, 24
+    ring = kv.KVRing(1, 1, 64, R, T, max_position=R + 42 * T, host_only=True, rope_3d=(S, 4, 0, 0))
+    with pytest.raises(kv.KVRingError) as e:
+        ring.write(0, None, None, n_tokens=13)
+    assert e.value.code == kv.KVRING_EINVAL and "frames" in e.value.message
+    o = WriteTimeRing(R, 1, 2)
+    z = np.zeros((T, 1, 2), np.float32)
+    for s in range(60):
+        if s > 0 and s % 42 == 0:
+            ring.rebase()
+            assert o.rebase() % S == 0
+        n = T if s % 3 else S
+        ring.write(0, None, None, n_tokens=n)
+        o.write(z[:n], z[:n])
+        _compare(ring, 0, o)

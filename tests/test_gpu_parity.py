@@ -273,6 +273,82 @@ def test_naive_upkeep_production_sampled():
     assert_attention_close(out[np.ix_(rows, heads)], ref, "naive production")
 
 
+def _layout_3d(d, S, W):
+    ph = d // 6
+    return (S, W, d // 2 - 2 * ph, ph)
+
+
+@pytest.mark.parametrize("R,T,H,d", [(96, 24, 2, 64), (96, 36, 2, 128)])
+def test_rope_3d_small(R, T, H, d):
+    """3-D video RoPE (frames of 12 tokens, rows of 4): writes through wraps, attention,
+    and resets by whole frames that turn only the time band."""
+    S, W = 12, 4
+    lay = _layout_3d(d, S, W)
+    ring = kv.KVRing(1, H, d, R, T, max_position=R + 6 * T, rope_3d=lay)
+    o = WriteTimeRing(R, H, d, layout=lay)
+    for s in range(14):
+        if s > 0 and s % 6 == 0:
+            before = ring.snapshot(0)["k"].copy()
+            ring.rebase()
+            o.rebase()
+            fk, fv = _check_cache(ring, 0, o)
+            assert fk == 1.0 and fv == 1.0
+            after = ring.snapshot(0)["k"]
+            assert np.array_equal(after[..., 2 * lay[2]:], before[..., 2 * lay[2]:])
+        kb, kf = chunk_pair("k", 1100 + s, T, H, d, True)
+        vb, vf = chunk_pair("v", 1100 + s, T, H, d, True)
+        ring.write(0, to_dev(kb), to_dev(vb))
+        o.write(kf, vf)
+        fk, fv = _check_cache(ring, 0, o)
+        assert fk == 1.0 and fv == 1.0
+        qb, qf = chunk_pair("q", 1100 + s, T, H, d, True)
+        assert_attention_close(ring.attend(0, to_dev(qb)).cpu().numpy(), o.attend(qf), f"3-D step {s}")
+
+
+def test_rope_3d_naive_refresh():
+    """Naive ring with 3-D RoPE: every refresh equals the oracle's re-rotation."""
+    from oracle.schemes import NaiveWindow
+    R, T, H, d, S, W = 96, 24, 2, 128, 12, 4
+    lay = _layout_3d(d, S, W)
+    ring = kv.KVRing(1, H, d, R, T, max_position=R + 6 * T, naive_upkeep=True, rope_3d=lay)
+    o = NaiveWindow(R, H, d, layout=lay)
+    for s in range(12):
+        if s > 0 and s % 6 == 0:
+            ring.rebase()
+            o.rebase()
+        kb, kf = chunk_pair("k", 1200 + s, T, H, d, True)
+        vb, vf = chunk_pair("v", 1200 + s, T, H, d, True)
+        ring.write(0, to_dev(kb), to_dev(vb))
+        o.write(kf, vf)
+        ring.naive_refresh(0)
+        _check_naive(ring, 0, o, f"3-D step {s}")
+
+
+def test_rope_3d_production_frames_sampled():
+    """Frames of 11 x 17 = 187 tokens, 4 frames per chunk (748 tokens), a 31-frame ring
+    (5,797 slots), 16 heads x 128: fill, reset, then cache bytes and sampled attention."""
+    S, W, H, d = 187, 17, 16, 128
+    T, R = 4 * S, 31 * S
+    lay = _layout_3d(d, S, W)
+    ring = kv.KVRing(1, H, d, R, T, max_position=R + 42 * T, rope_3d=lay)
+    o = WriteTimeRing(R, H, d, layout=lay)
+    for w in range(9):
+        kb, kf = chunk_pair("k", 1300 + w, T, H, d, True)
+        vb, vf = chunk_pair("v", 1300 + w, T, H, d, True)
+        ring.write(0, to_dev(kb), to_dev(vb))
+        o.write(kf, vf)
+    ring.rebase()
+    assert o.rebase() % S == 0
+    fk, fv = _check_cache(ring, 0, o)
+    assert fk == 1.0 and fv == 1.0
+    qb, qf = chunk_pair("q", 1310, T, H, d, True)
+    out = ring.attend(0, to_dev(qb)).cpu().numpy()
+    rng = np.random.default_rng(17)
+    heads = np.array([2, 9, 15])
+    rows = np.unique(np.concatenate([rng.choice(T, 40, replace=False), [0, 186, 187, 747]]))
+    assert_attention_close(out[np.ix_(rows, heads)], o.attend(qf, heads=heads, rows=rows), "3-D production")
+
+
 def test_edge_sizes():
     # T = 1, T = R (whole ring in one write), then a write that wraps mid-group
     R, H, d = 40, 1, 64

@@ -207,6 +207,9 @@ def test_3d_reset_rotates_only_the_time_band():
     assert np.mean(ring.k8[..., :24] != before[..., :24]) > 0.3
     k8, _, _, _ = naive.cache_codes()
     idx = (ring.head - ring.count + np.arange(ring.count)) % R
+    # a whole-frame shift leaves height and width as they were: those codes equal a
+    # fresh rotation at the shifted positions exactly
+    assert np.array_equal(ring.k8[:, idx, 24:], k8.transpose(1, 0, 2)[..., 24:])
     from oracle import e4m3
     a = e4m3.decode(ring.k8[:, idx])
     b = e4m3.decode(k8.transpose(1, 0, 2))
