@@ -285,17 +285,47 @@ def oracle_sample(cfg, seconds_hint=20.0):
 # DRAM bytes (read + write) per attend_kernel launch, from the ncu capture summarised
 # in profiles/attend_kernel_production_ring_8_blocks.md; valid only for the attention
 # source it was taken on (sha256 prefix), else reported as null.
-ATTEND_TRAFFIC = {"bytes": 27.05e6, "source_sha256": "f0d027049025621d"}
+ATTEND_TRAFFIC = {"bytes": 27.05e6, "source_sha256": "f0d027049025621d",
+                  "shape": {"H": 16, "d": 128, "R": 5788, "T": 757}}
 
 
-def attend_traffic():
+def attend_traffic(cfg):
     import hashlib
+    if any(cfg[k] != v for k, v in ATTEND_TRAFFIC["shape"].items()):
+        return None
     path = os.path.join(ROOT, "kv_cache_gb300", "csrc", "k_attend.cu")
     try:
         digest = hashlib.sha256(open(path, "rb").read()).hexdigest()
     except OSError:
         return None
     return ATTEND_TRAFFIC["bytes"] if digest.startswith(ATTEND_TRAFFIC["source_sha256"]) else None
+
+
+def probe_peaks(n=8192, iters=20):
+    """Library GEMM throughput on this GPU, FP8 e4m3 (per-tensor scales) and bf16 (a yardstick only)."""
+    import torch
+    dev = torch.device("cuda", 0)
+    a16 = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    b16 = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    a8 = a16.to(torch.float8_e4m3fn)
+    b8 = b16.to(torch.float8_e4m3fn).t().contiguous().t()     # column-major second operand
+    one = torch.ones((), device=dev, dtype=torch.float32)
+    runs = {"fp8": lambda: torch._scaled_mm(a8, b8, scale_a=one, scale_b=one, out_dtype=torch.bfloat16),
+            "bf16": lambda: a16 @ b16}
+    out = {"probe": "gemm", "n": n}
+    for name, fn in runs.items():
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(iters):
+            fn()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        out[f"{name}_tflops"] = 2.0 * n ** 3 * iters / (e0.elapsed_time(e1) * 1e-3) / 1e12
+    out["fp8_over_bf16"] = out["fp8_tflops"] / out["bf16_tflops"]
+    return out
 
 
 def algorithmic(cfg):
@@ -314,6 +344,11 @@ def main():
     ap.add_argument("--impl", default="kvring", choices=["kvring", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--small", action="store_true", help="4 blocks instead of 60 (quick checks)")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="number of heads (64 = the unsharded model width; default 16, one tensor-parallel shard)")
+    ap.add_argument("--probe-peaks", action="store_true",
+                    help="time an 8192^3 FP8 (torch._scaled_mm) and bf16 GEMM on this GPU and print their ratio, "
+                         "the check of the FP8 = 2 x bf16 roofline denominator")
     ap.add_argument("--blocks", type=int, default=0,
                     help="number of blocks (profiling cases; 8 blocks already keep one layer's ring out of L2 "
                          "between its visits)")
@@ -325,6 +360,12 @@ def main():
                     help="passes 1..3 rewrite the newest chunk with new K/V (kvring_write_ex, no advance)")
     args = ap.parse_args()
     cfg = dict(SMALL if args.small else WORKLOAD)
+    if args.probe_peaks:
+        print(json.dumps(probe_peaks()))
+        return
+    if args.heads > 0:
+        cfg["name"] = cfg["name"].replace("60 blocks", f"60 blocks of {args.heads} heads")
+        cfg["H"] = args.heads
     if args.blocks > 0:
         cfg["name"] = cfg["name"].replace(f"{cfg['L']} blocks", f"{args.blocks} blocks")
         cfg["L"] = args.blocks
@@ -392,7 +433,7 @@ def main():
                 "d2h_bytes_per_step": r["d2h"], "steps": r["e2e_steps"]},
         "gpu_launches": r["launches"],
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": fp8_sustained, "unit": "TFLOP/s",
-                     "frac": attn_tflops / fp8_sustained, "traffic": attend_traffic(),
+                     "frac": attn_tflops / fp8_sustained, "traffic": attend_traffic(cfg),
                      "traffic_unit": "bytes per attend_kernel launch (ncu, 8-block run)",
                      "kernel": "attention call (q-prep + attention + split combine)",
                      "peak_source": f"{peak_src}: 2 x bf16_tflops_sustained (FP8 = 2 x bf16 nominal ratio)"},
