@@ -555,6 +555,7 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
         const float a = scale_of(__ldg(p.qamax + (size_t)h * p.Tstride + qrow)) * p.log2e_rsqrt_d;
         float gk[4], gl[4], gi[4];
         bool uni[2];
+        int kinds = 0;   // 8 bits per group of the current tile: its kind (0 = one range)
         const float* am = nullptr;
         const GroupInfo* info = nullptr;
         int slot0 = 0;
@@ -568,7 +569,7 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
             am = reinterpret_cast<const float*>(sAm + st * L::kAm);   // K amax [128], V amax [128]
             info = reinterpret_cast<const GroupInfo*>(sAm + st * L::kAm + L::kAmRows);
             if (!warp_wait(&bars[kBIF + st], (uint32_t)((ld / NST) & 1), sAbort, p, kWaitKVFull)) return false;
-            int kinds = 0;
+            kinds = 0;
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
                 const float4 i0 = reinterpret_cast<const float4*>(info + g)[0];
@@ -586,10 +587,15 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
             return fmaxf(fmaf(max32(ra), hb ? gk[2] : gk[0], hb ? gl[2] : gl[0]),
                          fmaf(max32(rb), hb ? gk[3] : gk[1], hb ? gl[3] : gl[1]));
         };
-        // the same for any groups, read again from tensor memory at taddr (half hb)
-        auto zmax2_general = [&](uint32_t taddr, int hb) -> float {
-            return fmaxf(zmax_general(taddr, info, am, 2 * hb, slot0, p.count, a, lane),
-                         zmax_general(taddr + 32, info, am, 2 * hb + 1, slot0, p.count, a, lane));
+        auto one_range = [&](int g) -> bool { return ((kinds >> (8 * g)) & 3) == 0; };
+        // the same when a group of the half is not one range: that group is read
+        // again from tensor memory at taddr (+ 32) on the general path
+        auto zmax2_mixed = [&](const uint32_t (&ra)[32], const uint32_t (&rb)[32], uint32_t taddr, int hb) -> float {
+            const float za = one_range(2 * hb) ? fmaf(max32(ra), hb ? gk[2] : gk[0], hb ? gl[2] : gl[0])
+                                               : zmax_general(taddr, info, am, 2 * hb, slot0, p.count, a, lane);
+            const float zb = one_range(2 * hb + 1) ? fmaf(max32(rb), hb ? gk[3] : gk[1], hb ? gl[3] : gl[1])
+                                                   : zmax_general(taddr + 32, info, am, 2 * hb + 1, slot0, p.count, a, lane);
+            return fmaxf(za, zb);
         };
         // First pass, one full tile at a time in S buffer j % 2 (S_q or, while it is
         // unused, O_q's columns): the row max M of z.
@@ -606,7 +612,7 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                 tmem_ld32_async(tSj + 32, rb);
                 tmem_wait_ld_dep(ra);
                 tmem_dep(rb);
-                tz = uni[0] ? zmax2(ra, rb, 0) : zmax2_general(tSj, 0);
+                tz = uni[0] ? zmax2(ra, rb, 0) : zmax2_mixed(ra, rb, tSj, 0);
             }
             {
                 uint32_t ra[32], rb[32];
@@ -621,7 +627,7 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                     mbar_arrive_warp(&bars[kBPF1 + 2 * q + b]);
                     tz = fmaxf(tz, zmax2(ra, rb, 1));
                 } else {
-                    tz = fmaxf(tz, zmax2_general(tSj + 64, 1));
+                    tz = fmaxf(tz, zmax2_mixed(ra, rb, tSj + 64, 1));
                     tc_fence_before();
                     __syncwarp();
                     mbar_arrive_warp(&bars[kBPF1 + 2 * q + b]);
@@ -664,9 +670,21 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                     lsum += p_one_range(rb, hb ? gk[3] : gk[1], (hb ? gl[3] : gl[1]) - M, max32(rb), hb ? gi[3] : gi[1], pk);
                     tmem_st16(tSb + 16, pk);
                 } else {
-                    // group g0's P goes to columns [0, 16) before group g0 + 1 reads [32, 64)
-                    lsum = p_general(tSb, tSb, info, am, g0, slot0, p.count, a, M, lane);
-                    lsum += p_general(tSb + 32, tSb + 16, info, am, g0 + 1, slot0, p.count, a, M, lane);
+                    // each group on its own path; group g0's P goes to columns [0, 16)
+                    // before group g0 + 1 is (re)read from [32, 64)
+                    uint32_t pk[16];
+                    if (one_range(g0)) {
+                        lsum = p_one_range(ra, hb ? gk[2] : gk[0], (hb ? gl[2] : gl[0]) - M, max32(ra), hb ? gi[2] : gi[0], pk);
+                        tmem_st16(tSb, pk);
+                    } else {
+                        lsum = p_general(tSb, tSb, info, am, g0, slot0, p.count, a, M, lane);
+                    }
+                    if (one_range(g0 + 1)) {
+                        lsum += p_one_range(rb, hb ? gk[3] : gk[1], (hb ? gl[3] : gl[1]) - M, max32(rb), hb ? gi[3] : gi[1], pk);
+                        tmem_st16(tSb + 16, pk);
+                    } else {
+                        lsum += p_general(tSb + 32, tSb + 16, info, am, g0 + 1, slot0, p.count, a, M, lane);
+                    }
                 }
                 l_run += lsum;
                 // P_q(u) handed over once all 32 lanes' stores are done: one arrival per warp
