@@ -319,7 +319,7 @@ def oracle_sample(cfg, seconds_hint=20.0):
 # DRAM bytes (read + write) per attend_kernel launch, from the ncu capture summarised
 # in profiles/attend_kernel_production_ring_8_blocks.md; valid only for the attention
 # source it was taken on (sha256 prefix), else reported as null.
-ATTEND_TRAFFIC = {"bytes": 27.05e6, "source_sha256": "f0d027049025621d",
+ATTEND_TRAFFIC = {"bytes": 27.11e6, "source_sha256": "c5f50324d2760d7a",
                   "shape": {"H": 16, "d": 128, "R": 5788, "T": 757}}
 
 
