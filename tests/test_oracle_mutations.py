@@ -135,6 +135,15 @@ def _pair_angles_full_width(p, d, theta=10000.0, layout=None):
 _ORIG_PAIR_ANGLES = rope_mod.pair_angles
 
 
+def _quantise_q_per_column(q, positions, d, theta, layout=None):
+    # scale per column (over tokens) instead of per (token, head) row
+    qr = rope_mod.rotate_at(np.asarray(q, dtype=np.float32), positions, d, theta, layout)
+    amax = np.abs(qr).max(axis=0, keepdims=True).astype(np.float32)
+    _, inv = schemes_mod.scale_inv(amax)
+    codes = schemes_mod.quantise(qr, inv)
+    return codes, np.broadcast_to(np.abs(qr).max(axis=2), qr.shape[:2]).astype(np.float32)
+
+
 CASES = [
     ("rotation sign", [(rope_mod, "rotate", _rotate_sign_flipped)], t_rope.test_unit_vector_rotates_to_cos_sin),
     ("rotate-half pairing", [(rope_mod, "rotate", _rotate_halves)], t_rope.test_matches_complex_multiplication),
@@ -146,6 +155,7 @@ CASES = [
     ("ring head drift", [(t_ring, "WriteTimeRing", _RingOffByOne)], lambda: t_ring.test_logical_order_equals_shifted_window(96, 32)),
     ("3-D height/width swapped", [(rope_mod, "coords_3d", _coords_swapped)], t_rope.test_3d_each_band_is_1d_rope_at_its_coordinate),
     ("3-D band frequencies", [(rope_mod, "pair_angles", _pair_angles_full_width)], t_rope.test_3d_each_band_is_1d_rope_at_its_coordinate),
+    ("Q scale per column", [(schemes_mod, "quantise_q", _quantise_q_per_column)], t_sch.test_q_rows_reach_the_top_code_and_stay_within_half_a_step),
     ("rewrite slots", [(t_ring, "WriteTimeRing", _RewriteNextSlots)], lambda: t_ring.test_rewrite_equals_writing_that_chunk(10, 4, 3)),
     ("rewrite positions", [(t_ring, "WriteTimeRing", _RewriteNextPositions)], t_ring.test_rewrite_after_reset_uses_the_shifted_positions),
     ("rewrite stale scale", [(t_ring, "WriteTimeRing", _RewriteStaleScale)], lambda: t_ring.test_rewrite_equals_writing_that_chunk(12, 4, 3)),

@@ -158,3 +158,45 @@ def test_rebase_after_partial_fill_and_twice():
     assert d1 == 120 - 64 and d2 == 0
     k8, _, _, _ = naive.cache_codes()
     assert _pair_ulp_diff(_logical(ring, ring.k8), k8.transpose(1, 0, 2)).max() <= 1.0
+
+
+def test_q_rows_reach_the_top_code_and_stay_within_half_a_step():
+    # each (token, head) row of Q is scaled so that its largest rotated |value|
+    # lands on the top code (448), and every dequantised value is within half an
+    # e4m3 step of the rotated value (the RoPE routine is pinned on its own)
+    from oracle import e4m3, rope
+    from oracle.schemes import quantise_q, dequantised_q
+    rng = np.random.default_rng(31)
+    T, H, d = 40, 3, 64
+    q = (rng.standard_normal((T, H, d)) * rng.choice([0.01, 1.0, 30.0], size=(T, H, 1))).astype(np.float32)
+    q[5, 1] = 0.0                                           # an all-zero row
+    pos = np.arange(100, 100 + T)
+    codes, amax = quantise_q(q, pos, d, 10000.0)
+    mags = np.abs(e4m3.decode(codes))
+    top = mags.max(axis=2)
+    assert top[5, 1] == 0.0 and amax[5, 1] == 0.0
+    nz = np.ones((T, H), bool)
+    nz[5, 1] = False
+    assert np.all(top[nz] == 448.0)
+    qr = rope.rotate_at(q, pos, d).astype(np.float64)
+    deq = dequantised_q(q, pos, d, 10000.0)
+    scale = (amax.astype(np.float64) / 448.0)[..., None]
+    step = e4m3.ulp_at(np.abs(qr) / np.where(scale > 0, scale, 1.0)) * scale
+    assert np.all(np.abs(deq - qr) <= 0.5 * step * (1 + 1e-6) + 1e-30)
+
+
+def test_dequantisers_are_exact_products():
+    # fl32(decode * scale) is the float32 rounding of the exact product, and the
+    # float64 form is the exact product itself (two float32 factors)
+    from fractions import Fraction
+    from oracle import e4m3
+    from oracle.schemes import dequantise_f32, dequantise_f64
+    rng = np.random.default_rng(32)
+    codes = rng.integers(0, 256, size=400).astype(np.uint8)
+    codes = codes[(codes & 0x7F) != 0x7F]                   # no NaN codes
+    scale = (rng.random(codes.shape) * 3 + 1e-3).astype(np.float32)
+    exact = [Fraction(float(e4m3.decode(np.array([c]))[0])) * Fraction(float(s)) for c, s in zip(codes, scale)]
+    f64 = dequantise_f64(codes, scale)
+    assert all(Fraction(float(v)) == x for v, x in zip(f64, exact))
+    f32 = dequantise_f32(codes, scale)
+    assert all(np.float32(float(x)) == v for v, x in zip(f32, exact))
