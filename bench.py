@@ -286,6 +286,41 @@ def run_gpu(args, cfg, rank, world):
                 e2e_ms=e2e_ms, e2e_steps=e2e_steps, h2d=h2d // e2e_steps, d2h=d2h // e2e_steps)
 
 
+def run_rebase_stress(args, cfg, rounds=10):
+    """Position-reset stress: the rings filled, then `rounds` resets, each after one
+    more chunk per block (so every layer has a delta); only the rebases are timed."""
+    import torch
+    from kv_cache_gb300 import kvring as kv
+    from kv_cache_gb300 import synthetic
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    L, H, d, R, T = (cfg[k] for k in ("L", "H", "d", "R", "T"))
+    ring = kv.KVRing(L, H, d, R, T, max_position=R + 42 * T)
+    _, pool = make_pool(cfg, torch, device)
+    stream = torch.cuda.current_stream(device)
+    for w in range(41):                      # 41 steps of writes: full rings, positions far from 0
+        for l in range(L):
+            i = synthetic.pool_index(w, l, 4, L)
+            ring.write(l, pool["k"][i], pool["v"][i], stream=stream)
+    ts = []
+    for r in range(rounds + 1):
+        if r > 0:
+            for l in range(L):
+                i = synthetic.pool_index(41 + r, l, 4, L)
+                ring.write(l, pool["k"][i], pool["v"][i], stream=stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ring.rebase(stream)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        if r > 0:                            # the first reset (delta 41 chunks) is a warm-up
+            ts.append(e0.elapsed_time(e1))
+    if ring.check_device(stream) != kv.KVRING_OK:
+        raise RuntimeError(kv.kvring_last_error(ring.handle))
+    ring.close()
+    return ts
+
+
 def oracle_sample(cfg, seconds_hint=20.0):
     """Time the CPU oracle on one block: a full window of writes, then one step's write + 4 calls."""
     from kv_cache_gb300 import synthetic
@@ -393,6 +428,8 @@ def main():
     ap.add_argument("--small", action="store_true", help="4 blocks instead of 60 (quick checks)")
     ap.add_argument("--heads", type=int, default=0,
                     help="number of heads (64 = the unsharded model width; default 16, one tensor-parallel shard)")
+    ap.add_argument("--rebase-stress", action="store_true",
+                    help="the reset stress workload: full rings, then 10 timed resets (one JSON line)")
     ap.add_argument("--probe-peaks", action="store_true",
                     help="time an 8192^3 FP8 (torch._scaled_mm) and bf16 GEMM on this GPU and print their ratio, "
                          "the check of the FP8 = 2 x bf16 roofline denominator")
@@ -407,15 +444,31 @@ def main():
                     help="passes 1..3 rewrite the newest chunk with new K/V (kvring_write_ex, no advance)")
     args = ap.parse_args()
     cfg = dict(SMALL if args.small else WORKLOAD)
-    if args.probe_peaks:
-        print(json.dumps(probe_peaks()))
-        return
     if args.heads > 0:
         cfg["name"] = cfg["name"].replace("60 blocks", f"60 blocks of {args.heads} heads")
         cfg["H"] = args.heads
     if args.blocks > 0:
         cfg["name"] = cfg["name"].replace(f"{cfg['L']} blocks", f"{args.blocks} blocks")
         cfg["L"] = args.blocks
+    if args.probe_peaks:
+        print(json.dumps(probe_peaks()))
+        return
+    if args.rebase_stress:
+        ts = run_rebase_stress(args, cfg)
+        peaks, peak_src = load_peaks()
+        med = statistics.median(ts)
+        nbytes = 2.0 * cfg["L"] * cfg["H"] * cfg["R"] * cfg["d"]
+        print(json.dumps({
+            "metric": "rebase ms (position reset of every cached K)", "value": med, "unit": "ms",
+            "higher_is_better": False, "n_gpus": 1, "steps": len(ts), "dtype": "fp8_e4m3", "data": "synthetic",
+            "config": {"workload": f"reset stress: {cfg['L']} blocks x {cfg['H']} heads x {cfg['d']}, "
+                                   f"R={cfg['R']}, filled over 41 steps, then {len(ts)} resets",
+                       "l2": f"{nbytes / 1e9:.2f} GB of K codes read and written per reset (larger than L2)"},
+            "samples_ms": ts, "min_ms": min(ts),
+            "roofline": {"bound": "hbm", "achieved": nbytes / (med * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": nbytes / (med * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                         "peak_source": peak_src}}))
+        return
     cfg["writes_per_step"] = cfg["passes"] if args.rewrite_per_pass else 1
     cfg["naive_upkeep"] = bool(args.naive_upkeep)
     if args.rewrite_per_pass:
