@@ -39,11 +39,13 @@ namespace kvring_impl {
 // e4m3 with its own amax, write [H][Tstride][d] codes + [H][Tstride] amax.
 // Rows T..Tpad-1 are written as zeros.
 __global__ void __launch_bounds__(128) qprep_kernel(const __grid_constant__ QPrepParams p) {
-    // the attention kernel that follows may start its own set-up (it waits for
-    // this grid before it touches Q); this grid itself may have started before
-    // the one ahead of it finished, so it waits for it before reading anything
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // This grid may have started before the one ahead of it finished, so it
+    // waits for it before reading anything.  Only then may the attention grid
+    // that follows start: that grid loads its first K/V tiles before its own
+    // wait, so the ring must be final (the write ahead of this grid complete)
+    // by the time any of its blocks exists.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int d = p.d;
     const int tpr = d / 8;                       // threads per row, 8 elements each
     const int rows_per_block = 128 / tpr;
@@ -765,7 +767,9 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
         for (int ld = 0; ld < 2 * nt; ++ld) {
             if (ld == (nt < NST ? nt : NST)) {
                 // the query tiles, once the first stages are on their way and Q prep
-                // (the grid before this one) has finished
+                // (the grid before this one) has finished; the stages above could
+                // be issued earlier because this grid starts only after Q prep has
+                // waited for the grid before it (the write of the ring)
                 asm volatile("griddepcontrol.wait;" ::: "memory");
                 mbar_expect_tx_warp(&bars[kBQ], (uint32_t)(nq * L::kQ));
                 tma_load_3d_warp(sQ, &maps.q8, &bars[kBQ], 0, (2 * pair) * 128, h);
@@ -1031,7 +1035,9 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
 
 // Launched with programmatic stream serialisation: its CTAs may start while the
 // Q prep grid before it is still running; they wait for it (griddepcontrol.wait)
-// before reading Q.
+// before reading Q.  Their first K/V loads come before that wait: Q prep lets
+// this grid start only after its own wait, so whatever wrote the ring before Q
+// prep has finished by then.
 cudaError_t launch_attend(const AttendParams& p, const AttendMaps& maps, cudaStream_t s) {
     const int grid = p.H * p.npairs * p.splits;
     const int smem = p.d == 128 ? (int)AttendSmem<128>::kAlloc : (int)AttendSmem<64>::kAlloc;
