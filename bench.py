@@ -354,7 +354,7 @@ def oracle_sample(cfg, seconds_hint=20.0):
 # DRAM bytes (read + write) per attend_kernel launch, from the ncu capture summarised
 # in profiles/attend_kernel_production_ring_8_blocks.md; valid only for the attention
 # source it was taken on (sha256 prefix), else reported as null.
-ATTEND_TRAFFIC = {"bytes": 27.11e6, "source_sha256": "c5f50324d2760d7a",
+ATTEND_TRAFFIC = {"bytes": 27.11e6, "source_sha256": "3718144c614ef9ba",
                   "shape": {"H": 16, "d": 128, "R": 5788, "T": 757}}
 
 
