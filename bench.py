@@ -28,6 +28,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -63,7 +64,7 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"kvring_bench_clocks_gpu{index}_{os.getpid()}.csv")
 
     def start(self):
         try:
@@ -98,6 +99,10 @@ class ClockSampler:
             for n, v in zip(names, parts[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
         load = [x for x in sm if smax and x > 0.5 * smax] or sm
         return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": smax,
                 "reasons": sorted(reasons), "samples": len(sm)}
