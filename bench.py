@@ -42,6 +42,10 @@ WORKLOAD = dict(name="steady denoise step: 60 blocks x (1 write + 4 attention ca
                 L=60, H=16, d=128, R=5788, T=757, passes=4, reset_every=42)
 SMALL = dict(name="small check: 4 blocks x (1 write + 4 attention calls)", L=4, H=16, d=128, R=5788, T=757,
              passes=4, reset_every=42)
+# 3-D (time, height, width) video RoPE: frames of 11 x 17 latent tokens, writes of 4
+# frames (748 tokens), a ring of 31 frames (5,797 slots, the nearest whole-frame
+# size to 5,788); band split 22 / 21 / 21 pairs of d = 128 (time / height / width).
+ROPE_3D = dict(T=748, R=5797, rope_3d=(187, 17, 22, 21))
 
 
 def load_peaks():
@@ -127,7 +131,7 @@ def run_gpu(args, cfg, rank, world):
     L, H, d, R, T, P, RE = (cfg[k] for k in ("L", "H", "d", "R", "T", "passes", "reset_every"))
     WP = cfg["writes_per_step"]           # 1, or P when every pass rewrites the newest chunk
     NV = cfg.get("naive_upkeep", False)   # the comparison scheme: refresh the whole window per call
-    ring = kv.KVRing(L, H, d, R, T, max_position=R + RE * T, naive_upkeep=NV)
+    ring = kv.KVRing(L, H, d, R, T, max_position=R + RE * T, naive_upkeep=NV, rope_3d=cfg.get("rope_3d"))
     host, pool = make_pool(cfg, torch, device)
     stream = torch.cuda.current_stream(device)
     outs = [torch.empty((T, H, d), dtype=torch.float32, device=device) for _ in range(P)]
@@ -300,7 +304,7 @@ def run_rebase_stress(args, cfg, rounds=10):
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     L, H, d, R, T = (cfg[k] for k in ("L", "H", "d", "R", "T"))
-    ring = kv.KVRing(L, H, d, R, T, max_position=R + 42 * T)
+    ring = kv.KVRing(L, H, d, R, T, max_position=R + 42 * T, rope_3d=cfg.get("rope_3d"))
     _, pool = make_pool(cfg, torch, device)
     stream = torch.cuda.current_stream(device)
     for w in range(41):                      # 41 steps of writes: full rings, positions far from 0
@@ -332,7 +336,7 @@ def oracle_sample(cfg, seconds_hint=20.0):
     from oracle.schemes import NaiveWindow
 
     L, H, d, R, T, P = (cfg[k] for k in ("L", "H", "d", "R", "T", "passes"))
-    naive = NaiveWindow(R, H, d)
+    naive = NaiveWindow(R, H, d, layout=cfg.get("rope_3d"))
     f32 = synthetic.bf16_to_f32
     fill = -(-R // T)
     for w in range(fill):
@@ -352,14 +356,14 @@ def oracle_sample(cfg, seconds_hint=20.0):
     threads = os.cpu_count()
     return dict(block_s=block_s, step_s=step_s, cores=threads,
                 sample=f"one block (1 write + {WP - 1} rewrites + {P} attention calls, naive per-call upkeep, "
-                       f"float64 attention) "
+                       f"float64 attention{', 3-D RoPE' if cfg.get('rope_3d') else ''}) "
                        f"at {H} heads x {d}, R={R}, T={T}; x{L} blocks (extrapolated)")
 
 
 # DRAM bytes (read + write) per attend_kernel launch, from the ncu capture summarised
 # in profiles/attend_kernel_production_ring_8_blocks.md; valid only for the attention
 # source it was taken on (sha256 prefix), else reported as null.
-ATTEND_TRAFFIC = {"bytes": 27.11e6, "source_sha256": "3718144c614ef9ba",
+ATTEND_TRAFFIC = {"bytes": 26.79e6, "source_sha256": "efdf3becdebff800",
                   "shape": {"H": 16, "d": 128, "R": 5788, "T": 757}}
 
 
@@ -415,11 +419,20 @@ def probe_peaks(n=8192, iters=20):
     return out
 
 
+def rebase_row_bytes(cfg):
+    """Bytes of one cached K row that a reset reads (and writes back): the whole row
+    in 1-D; with 3-D RoPE only the 16-byte pieces that hold time-band pairs."""
+    if not cfg.get("rope_3d"):
+        return cfg["d"]
+    pt = cfg["rope_3d"][2]
+    return -(-pt // 8) * 16
+
+
 def algorithmic(cfg):
     L, H, d, R, T, P = (cfg[k] for k in ("L", "H", "d", "R", "T", "passes"))
     write_bytes = T * H * d * 2 * 2 + T * H * d * 2           # bf16 K,V in + e4m3 K,V out
     attend_flop = 4.0 * T * R * d * H
-    rebase_bytes = 2.0 * L * H * R * d                        # e4m3 K read + write, full rings
+    rebase_bytes = 2.0 * L * H * R * rebase_row_bytes(cfg)   # e4m3 K read + write, full rings
     return write_bytes, attend_flop, rebase_bytes
 
 
@@ -447,8 +460,14 @@ def main():
                          "all of it before every attention call (kvring_naive_refresh)")
     ap.add_argument("--rewrite-per-pass", action="store_true",
                     help="passes 1..3 rewrite the newest chunk with new K/V (kvring_write_ex, no advance)")
+    ap.add_argument("--rope-3d", action="store_true",
+                    help="3-D (time, height, width) video RoPE: frames of 11 x 17 tokens, 4-frame writes "
+                         "(748 tokens), a 31-frame ring (5,797 slots)")
     args = ap.parse_args()
     cfg = dict(SMALL if args.small else WORKLOAD)
+    if args.rope_3d:
+        cfg.update(ROPE_3D)
+        cfg["name"] = cfg["name"] + ", 3-D video RoPE (frames of 11 x 17 tokens, 4-frame writes of 748, 31-frame ring of 5,797)"
     if args.heads > 0:
         cfg["name"] = cfg["name"].replace("60 blocks", f"60 blocks of {args.heads} heads")
         cfg["H"] = args.heads
@@ -462,12 +481,14 @@ def main():
         ts = run_rebase_stress(args, cfg)
         peaks, peak_src = load_peaks()
         med = statistics.median(ts)
-        nbytes = 2.0 * cfg["L"] * cfg["H"] * cfg["R"] * cfg["d"]
+        nbytes = 2.0 * cfg["L"] * cfg["H"] * cfg["R"] * rebase_row_bytes(cfg)
         print(json.dumps({
             "metric": "rebase ms (position reset of every cached K)", "value": med, "unit": "ms",
             "higher_is_better": False, "n_gpus": 1, "steps": len(ts), "dtype": "fp8_e4m3", "data": "synthetic",
             "config": {"workload": f"reset stress: {cfg['L']} blocks x {cfg['H']} heads x {cfg['d']}, "
-                                   f"R={cfg['R']}, filled over 41 steps, then {len(ts)} resets",
+                                   f"R={cfg['R']}, filled over 41 steps, then {len(ts)} resets"
+                                   + (f", 3-D RoPE (frames of {cfg['rope_3d'][0]}; only the time band turns)"
+                                      if cfg.get("rope_3d") else ""),
                        "l2": f"{nbytes / 1e9:.2f} GB of K codes read and written per reset (larger than L2)"},
             "samples_ms": ts, "min_ms": min(ts),
             "roofline": {"bound": "hbm", "achieved": nbytes / (med * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],

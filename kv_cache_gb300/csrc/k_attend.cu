@@ -21,6 +21,12 @@
 //  * The V tile is widened from e4m3 to fp16 in shared memory (exact, as
 //    V * 2^-8) and O += P V runs on tcgen05 (kind::f16, M = 128, N = d, P from
 //    tensor memory); out = 2^8 O / l, or (2^8 O, M, l) per split for the merge.
+//  * The KV splits of a (head, query pair) merge in one of three ways, chosen
+//    on the host: as one thread-block cluster, reading each other's (O, M, l)
+//    from distributed shared memory, when every cluster fits on the device at
+//    once; else, with every CTA resident (cooperative launch), each split
+//    merging a share of the rows from the others' partials in global memory;
+//    else the last split to finish merging all rows.
 //  * Slots are walked in physical order 0..count-1: softmax attention does not
 //    depend on key order and each slot already carries its rotation, so the
 //    ring wrap needs no special case and no gather.
@@ -926,10 +932,74 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
         }
         return;
     }
-    // partial of this split: O * 2^8 (unnormalised) and (M, l) per row
+    constexpr int kRowsAtOnce = 4;
+    if (p.cluster) {
+        // The splits of this (head, pair) are the CTAs of one cluster (rank = split).
+        // Once all have their O and (M, l) in shared memory, each merges its share
+        // of the rows reading the others' shared memory directly: no partials in
+        // global memory, no counters.  Every thread of every CTA of the cluster
+        // reaches both barriers (aborted or not), so neither waits for ever.
+        cluster_sync_all();
+        const int r0 = split * rows / p.splits, r1 = (split + 1) * rows / p.splits;
+        uint32_t o_at[kMaxSplits], ml_at[kMaxSplits];
+#pragma unroll
+        for (int sp = 0; sp < kMaxSplits; ++sp) {
+            const uint32_t rank = (uint32_t)(sp < p.splits ? sp : 0);
+            o_at[sp] = dsmem_map(smem_u32(sO), rank);
+            ml_at[sp] = dsmem_map(smem_u32(sML), rank);
+        }
+        for (int rb = r0 + warp * kRowsAtOnce; rb < r1; rb += kRowsAtOnce * (kAttendThreads / 32)) {
+            float2 ml[kRowsAtOnce][kMaxSplits];
+            float4 o[kRowsAtOnce][kMaxSplits];
+#pragma unroll
+            for (int k = 0; k < kRowsAtOnce; ++k) {
+                const int rr = rb + k;
+                const bool mine = rr < r1 && pair * 256 + rr < p.T;
+#pragma unroll
+                for (int sp = 0; sp < kMaxSplits; ++sp) {
+                    ml[k][sp] = make_float2(-INFINITY, 0.f);
+                    o[k][sp] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (sp < p.splits && mine) {
+                        ml[k][sp] = dsmem_ld_f2(ml_at[sp] + (uint32_t)rr * 8u);
+                        if (lanes_d) o[k][sp] = dsmem_ld_f4(o_at[sp] + (uint32_t)(rr * kORow + 4 * lane) * 4u);
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kRowsAtOnce; ++k) {
+                const int t = pair * 256 + rb + k;
+                if (rb + k >= r1 || t >= p.T || !lanes_d) continue;
+                float mx = ml[k][0].x;
+#pragma unroll
+                for (int sp = 1; sp < kMaxSplits; ++sp) mx = fmaxf(mx, ml[k][sp].x);
+                float lw = 0.f;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int sp = 0; sp < kMaxSplits; ++sp) {
+                    const float w = sp < p.splits ? ex2_approx(ml[k][sp].x - mx) : 0.f;
+                    lw = fmaf(w, ml[k][sp].y, lw);
+                    acc.x = fmaf(w, o[k][sp].x, acc.x);
+                    acc.y = fmaf(w, o[k][sp].y, acc.y);
+                    acc.z = fmaf(w, o[k][sp].z, acc.z);
+                    acc.w = fmaf(w, o[k][sp].w, acc.w);
+                }
+                const float f = 256.f / lw;   // V was widened as V * 2^-8
+                *reinterpret_cast<float4*>(p.out + ((size_t)t * p.H + h) * D + 4 * lane) =
+                    make_float4(acc.x * f, acc.y * f, acc.z * f, acc.w * f);
+            }
+        }
+        // no CTA leaves while another may still read its shared memory
+        cluster_sync_all();
+        return;
+    }
+    // partial of this split: O * 2^8 (unnormalised) and (M, l) per row.  With a
+    // cooperative launch this split merges rows [own0, own1) itself and reads its
+    // own share of them from shared memory, so only the other rows go out.
+    const int own0 = p.coop ? split * rows / p.splits : 0;
+    const int own1 = p.coop ? (split + 1) * rows / p.splits : 0;
     for (int rr = warp; rr < rows; rr += kAttendThreads / 32) {
         const int t = pair * 256 + rr;
-        if (t >= p.T) continue;
+        if (t >= p.T || (rr >= own0 && rr < own1)) continue;
         const size_t pr = ((size_t)split * p.H + h) * p.Tstride + t;
         if (lanes_d) {
             const float4 o = *reinterpret_cast<const float4*>(sO + (size_t)rr * kORow + 4 * lane);
@@ -951,6 +1021,7 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
     int* done = p.counters + (size_t)p.H * (p.Tstride / 256) + unit;
     int r0 = 0, r1 = rows;
     if (p.coop) {
+        // own0 and own1 are this split's share of the rows
         if (tid == 0) {
             atomicAdd(counter, 1);
             const uint64_t t0 = globaltimer_ns();
@@ -969,8 +1040,8 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
             *sLast = ok;
         }
         __syncthreads();
-        r0 = split * rows / p.splits;
-        r1 = (split + 1) * rows / p.splits;
+        r0 = own0;
+        r1 = own1;
         if (!*sLast) r1 = r0;   // gave up: merge nothing
         __threadfence();
     } else {
@@ -979,7 +1050,6 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
         if (!*sLast) return;
         __threadfence();
     }
-    constexpr int kRowsAtOnce = 4;
     for (int rb = r0 + warp * kRowsAtOnce; rb < r1; rb += kRowsAtOnce * (kAttendThreads / 32)) {
         float2 ml[kRowsAtOnce][kMaxSplits];
         float4 o[kRowsAtOnce][kMaxSplits];
@@ -992,9 +1062,17 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
                 ml[k][sp] = make_float2(-INFINITY, 0.f);
                 o[k][sp] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (sp < p.splits && mine) {
-                    const size_t pr = ((size_t)sp * p.H + h) * p.Tstride + t;
-                    ml[k][sp] = __ldcg(reinterpret_cast<const float2*>(p.part_ml + pr * 2));
-                    if (lanes_d) o[k][sp] = __ldcg(reinterpret_cast<const float4*>(p.part_o + pr * D + 4 * lane));
+                    if (sp == split) {   // this split's own rows are still in its shared memory
+                        ml[k][sp] = sML[rb + k];
+                        if (lanes_d) {
+                            const float4 v = *reinterpret_cast<const float4*>(sO + (size_t)(rb + k) * kORow + 4 * lane);
+                            o[k][sp] = make_float4(v.x * 256.f, v.y * 256.f, v.z * 256.f, v.w * 256.f);
+                        }
+                    } else {
+                        const size_t pr = ((size_t)sp * p.H + h) * p.Tstride + t;
+                        ml[k][sp] = __ldcg(reinterpret_cast<const float2*>(p.part_ml + pr * 2));
+                        if (lanes_d) o[k][sp] = __ldcg(reinterpret_cast<const float4*>(p.part_o + pr * D + 4 * lane));
+                    }
                 }
             }
         }
@@ -1049,14 +1127,44 @@ cudaError_t launch_attend(const AttendParams& p, const AttendMaps& maps, cudaStr
     cfg.blockDim = dim3(kAttendThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[3];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     attr[1].id = cudaLaunchAttributeCooperative;   // the splits of a (head, pair) wait for each other
     attr[1].val.cooperative = p.coop ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
+    if (p.cluster) {   // consecutive CTAs are the splits of one (head, pair)
+        attr[2].id = cudaLaunchAttributeClusterDimension;
+        attr[2].val.clusterDim.x = (unsigned)p.splits;
+        attr[2].val.clusterDim.y = 1;
+        attr[2].val.clusterDim.z = 1;
+        cfg.numAttrs = 3;
+    }
     return cudaLaunchKernelEx(&cfg, kern, p, maps);
+}
+
+int attend_max_clusters(int d, int splits) {
+    const int smem = d == 128 ? (int)AttendSmem<128>::kAlloc : (int)AttendSmem<64>::kAlloc;
+    void (*kern)(AttendParams, AttendMaps) = d == 128 ? attend_kernel<128> : attend_kernel<64>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)splits, 1, 1);
+    cfg.blockDim = dim3(kAttendThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(kern), &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 }  // namespace kvring_impl

@@ -165,6 +165,7 @@ extern "C" int kvring_attend_noalloc(const void* k8, const void* vt8, const floa
     ap.timeout_ns = 2000000000LL;
     ap.skip_tile = -1;
     ap.coop = 0;
+    ap.cluster = 0;
 
     e = launch_qprep(qp, s);
     if (e == cudaSuccess) e = launch_attend(ap, maps, s);

@@ -44,6 +44,7 @@ struct kvring {
     int device = 0, num_sms = 0;
     int64_t Rpad = 0, Tstride = 0;
     int max_splits = 1;
+    int cluster_cap[5] = {-1, -1, -1, -1, -1};   // per split count: clusters the device holds at once (-1: not asked)
     int64_t resets = 0;
     std::vector<LayerState> layers;
     // device buffers (owned)
@@ -538,8 +539,18 @@ int kvring_attend(kvring_t* r, int32_t layer, const void* q, int32_t n_q, float*
     ap.log2e_rsqrt_d = (float)(1.4426950408889634 / std::sqrt((double)d));
     ap.timeout_ns = r->debug_timeout_ns > 0 ? r->debug_timeout_ns : 2000000000LL;
     ap.skip_tile = r->debug_skip_tile;
-    // with every CTA resident at once (one per SM), the splits merge together
-    ap.coop = (ap.splits > 1 && H * ap.npairs * ap.splits <= r->num_sms) ? 1 : 0;
+    // The splits of a (head, pair) merge through distributed shared memory when
+    // they can run as one cluster and every cluster fits on the device at once;
+    // else, with every CTA resident at once (one per SM), through global memory
+    // together; else the last split to finish merges them.
+    const int units = H * ap.npairs;
+    ap.cluster = 0;
+    if (ap.splits > 1 && ap.splits <= 4) {
+        int& cap = r->cluster_cap[ap.splits];
+        if (cap < 0) cap = attend_max_clusters(d, ap.splits);
+        ap.cluster = cap >= units ? 1 : 0;
+    }
+    ap.coop = (!ap.cluster && ap.splits > 1 && units * ap.splits <= r->num_sms) ? 1 : 0;
     r->debug_skip_tile = -1;
     r->debug_timeout_ns = 0;
     e = launch_attend(ap, r->maps, s);

@@ -122,6 +122,8 @@ struct AttendParams {
     long long timeout_ns;
     int skip_tile;            // testing aid: K/V load of this tile is not issued (-1 = off)
     int coop;                 // launched cooperatively: the splits of a (head, pair) merge together
+    int cluster;              // the splits of a (head, pair) are one thread-block cluster and merge
+                              // through distributed shared memory (no partials in global memory)
 };
 struct AttendMaps {
     CUtensorMap q8;           // 3-D {d, Tstride, H}
@@ -129,6 +131,8 @@ struct AttendMaps {
     CUtensorMap vt8;          // 3-D {Rpad, d, L*H}
 };
 cudaError_t launch_attend(const AttendParams& p, const AttendMaps& maps, cudaStream_t s);
+// How many clusters of `splits` attention CTAs (head dim d) the device holds at once (0 on error).
+int attend_max_clusters(int d, int splits);
 
 size_t attend_smem_bytes(int d);
 

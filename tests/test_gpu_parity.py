@@ -62,7 +62,8 @@ def test_write_production_shape():
     assert fk == 1.0 and fv == 1.0
 
 
-@pytest.mark.parametrize("R,T,H,d", [(96, 32, 2, 64), (100, 32, 2, 64), (300, 100, 2, 128)])
+# (600, 150, 2, 64): as the ring fills, 2, 3, 4 and 3 KV splits, merged as clusters
+@pytest.mark.parametrize("R,T,H,d", [(96, 32, 2, 64), (100, 32, 2, 64), (300, 100, 2, 128), (600, 150, 2, 64)])
 def test_attend_small(R, T, H, d):
     ring = kv.KVRing(1, H, d, R, T, max_position=4096)
     o = WriteTimeRing(R, H, d)
