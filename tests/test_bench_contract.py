@@ -30,3 +30,26 @@ def test_other_ranks_of_the_reference_arm_exit_without_work():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
                         "--warmup", "0"], capture_output=True, text=True, timeout=120, cwd=ROOT, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_workload_figures_and_the_3d_workload():
+    """The algorithmic figures the bench divides by, and the 3-D workload is one
+    the library accepts (whole frames per write and per ring)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from kv_cache_gb300 import kvring as kv
+    w = dict(bench.WORKLOAD)
+    write_bytes, attend_flop, rebase_bytes = bench.algorithmic(w)
+    assert write_bytes == 757 * 16 * 128 * 6                # bf16 K, V in + e4m3 K, V out
+    assert attend_flop == 4 * 757 * 5788 * 128 * 16          # Q K^T and P V, 2 FLOP per MAC
+    assert rebase_bytes == 2 * 60 * 16 * 5788 * 128          # e4m3 K read + written
+    c = dict(w)
+    c.update(bench.ROPE_3D)
+    S, W, pt, ph = c["rope_3d"]
+    assert c["T"] % S == 0 and c["R"] % S == 0 and S % W == 0
+    assert pt + 2 * ph == c["d"] // 2                        # width band as wide as the height band
+    assert bench.rebase_row_bytes(c) == 48                   # 22 time pairs = 44 bytes -> three 16-byte pieces
+    assert bench.rebase_row_bytes(w) == 128
+    ring = kv.KVRing(1, c["H"], c["d"], c["R"], c["T"], max_position=c["R"] + 42 * c["T"], host_only=True,
+                     rope_3d=c["rope_3d"])
+    ring.close()
