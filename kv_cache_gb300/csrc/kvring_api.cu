@@ -44,7 +44,7 @@ struct kvring {
     int device = 0, num_sms = 0;
     int64_t Rpad = 0, Tstride = 0;
     int max_splits = 1;
-    int cluster_cap[5] = {-1, -1, -1, -1, -1};   // per split count: clusters the device holds at once (-1: not asked)
+    int cluster_cap[5] = {0, 0, 0, 0, 0};   // per split count (2-4): attention clusters the device holds at once
     int64_t resets = 0;
     std::vector<LayerState> layers;
     // device buffers (owned)
@@ -331,6 +331,8 @@ int kvring_create(const kvring_config* cfg_in, kvring_t** out) {
     const int64_t L = cfg.num_layers, H = cfg.num_heads, d = cfg.head_dim;
     const int64_t ntiles_max = r->Rpad / 128, npairs_max = r->Tstride / 256;
     r->max_splits = (int)std::max<int64_t>(1, std::min<int64_t>(ntiles_max, (4 * r->num_sms + H * npairs_max - 1) / (H * npairs_max)));
+    // asked here, once, so that no attention call makes the occupancy query
+    for (int sp = 2; sp <= 4; ++sp) r->cluster_cap[sp] = attend_max_clusters((int)d, sp);
     const size_t ring_bytes = (size_t)(L * H * r->Rpad * d);
     const size_t amax_bytes = (size_t)(L * H * r->Rpad) * sizeof(float);
     const size_t rope_bytes = (size_t)cfg.max_position * (d / 2) * sizeof(float2);
@@ -545,11 +547,7 @@ int kvring_attend(kvring_t* r, int32_t layer, const void* q, int32_t n_q, float*
     // together; else the last split to finish merges them.
     const int units = H * ap.npairs;
     ap.cluster = 0;
-    if (ap.splits > 1 && ap.splits <= 4) {
-        int& cap = r->cluster_cap[ap.splits];
-        if (cap < 0) cap = attend_max_clusters(d, ap.splits);
-        ap.cluster = cap >= units ? 1 : 0;
-    }
+    if (ap.splits > 1 && ap.splits <= 4) ap.cluster = r->cluster_cap[ap.splits] >= units ? 1 : 0;
     ap.coop = (!ap.cluster && ap.splits > 1 && units * ap.splits <= r->num_sms) ? 1 : 0;
     r->debug_skip_tile = -1;
     r->debug_timeout_ns = 0;
