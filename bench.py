@@ -330,6 +330,19 @@ def run_rebase_stress(args, cfg, rounds=10):
     return ts
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu), for the CPU baseline's record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def oracle_sample(cfg, seconds_hint=20.0):
     """Time the CPU oracle on one block: a full window of writes, then one step's write + 4 calls."""
     from kv_cache_gb300 import synthetic
@@ -354,7 +367,7 @@ def oracle_sample(cfg, seconds_hint=20.0):
     block_s = time.perf_counter() - t0
     step_s = block_s * L
     threads = os.cpu_count()
-    return dict(block_s=block_s, step_s=step_s, cores=threads,
+    return dict(block_s=block_s, step_s=step_s, cores=threads, cpu_model=cpu_model(),
                 sample=f"one block (1 write + {WP - 1} rewrites + {P} attention calls, naive per-call upkeep, "
                        f"float64 attention{', 3-D RoPE' if cfg.get('rope_3d') else ''}) "
                        f"at {H} heads x {d}, R={R}, T={T}; x{L} blocks (extrapolated)")
@@ -522,7 +535,8 @@ def main():
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
                 "cpu_baseline": {"value": 1.0 / step_s, "unit": "steps/s", "cores": samples[0]["cores"],
-                                 "kind": "oracle", "sample": samples[0]["sample"]},
+                                 "cpu_model": samples[0]["cpu_model"], "kind": "oracle",
+                                 "sample": samples[0]["sample"]},
                 "e2e": {"value": 1.0 / step_s, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -575,7 +589,7 @@ def main():
     if not args.no_cpu_baseline:
         cb = oracle_sample(cfg)
         line["cpu_baseline"] = {"value": 1.0 / cb["step_s"], "unit": "steps/s", "cores": cb["cores"],
-                                "kind": "oracle", "sample": cb["sample"]}
+                                "cpu_model": cb["cpu_model"], "kind": "oracle", "sample": cb["sample"]}
     print(json.dumps(line))
 
 
