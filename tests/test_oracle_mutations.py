@@ -116,6 +116,52 @@ class _RewriteStaleScale(schemes_mod.WriteTimeRing):
         return slots
 
 
+def _rebase_planted(self, sign=-1, turn_v=False, rescale=False, shift_pos=True):
+    # the reset's steps (1-D) with one step made wrong
+    delta = self.next_pos - self.count
+    if delta != 0 and self.count > 0:
+        valid = np.nonzero(self.pos >= 0)[0]
+        c, s = rope_mod.angle_table([sign * delta], self.d, self.theta)
+        ks, ki = schemes_mod.scale_inv(self.kamax[:, valid])
+        x = schemes_mod.dequantise_f32(self.k8[:, valid, :], ks[..., None])
+        xr = rope_mod.rotate(x, c[0], s[0])
+        if rescale:   # a new scale from the rotated values instead of the frozen one
+            amax = np.abs(xr).max(axis=2).astype(np.float32)
+            _, ki = schemes_mod.scale_inv(amax)
+            self.kamax[:, valid] = amax
+        self.k8[:, valid, :] = schemes_mod.quantise(xr, ki[..., None])
+        if turn_v:
+            vs, vi = schemes_mod.scale_inv(self.vamax[:, valid])
+            y = schemes_mod.dequantise_f32(self.v8[:, valid, :], vs[..., None])
+            self.v8[:, valid, :] = schemes_mod.quantise(rope_mod.rotate(y, c[0], s[0]), vi[..., None])
+        if shift_pos:
+            self.pos[valid] -= delta
+    self.next_pos = self.count
+    self.last_pos -= delta
+    self.resets += 1
+    return int(delta)
+
+
+class _RebaseDeltaSign(schemes_mod.WriteTimeRing):
+    def rebase(self):
+        return _rebase_planted(self, sign=+1)
+
+
+class _RebaseTurnsV(schemes_mod.WriteTimeRing):
+    def rebase(self):
+        return _rebase_planted(self, turn_v=True)
+
+
+class _RebaseRescales(schemes_mod.WriteTimeRing):
+    def rebase(self):
+        return _rebase_planted(self, rescale=True)
+
+
+class _RebaseKeepsPositions(schemes_mod.WriteTimeRing):
+    def rebase(self):
+        return _rebase_planted(self, shift_pos=False)
+
+
 def _coords_swapped(p, S, W):
     t, s = divmod(int(p), S)
     return t, s % W, s // W
@@ -159,6 +205,14 @@ CASES = [
     ("rewrite slots", [(t_ring, "WriteTimeRing", _RewriteNextSlots)], lambda: t_ring.test_rewrite_equals_writing_that_chunk(10, 4, 3)),
     ("rewrite positions", [(t_ring, "WriteTimeRing", _RewriteNextPositions)], t_ring.test_rewrite_after_reset_uses_the_shifted_positions),
     ("rewrite stale scale", [(t_ring, "WriteTimeRing", _RewriteStaleScale)], lambda: t_ring.test_rewrite_equals_writing_that_chunk(12, 4, 3)),
+    ("rebase delta sign", [(t_sch, "WriteTimeRing", _RebaseDeltaSign)],
+     lambda: t_sch.test_rebase_within_one_pair_step_of_fresh_rotation(96, 32, 2, 64)),
+    ("rebase turns V", [(t_sch, "WriteTimeRing", _RebaseTurnsV)],
+     lambda: t_sch.test_rebase_within_one_pair_step_of_fresh_rotation(96, 32, 2, 64)),
+    ("rebase re-scales K", [(t_ring, "WriteTimeRing", _RebaseRescales)],
+     t_ring.test_reset_keeps_scales_and_rebases_positions_to_the_window),
+    ("rebase keeps positions", [(t_ring, "WriteTimeRing", _RebaseKeepsPositions)],
+     t_ring.test_reset_keeps_scales_and_rebases_positions_to_the_window),
 ]
 
 

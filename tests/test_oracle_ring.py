@@ -113,6 +113,24 @@ def test_scale_frozen_through_eviction():
     assert np.all(ring.kamax[:, 7] == chunk_amax_k(chunks[1]))
 
 
+def test_reset_keeps_scales_and_rebases_positions_to_the_window():
+    """A reset keeps every slot's frozen K and V scale and chunk id (scales are
+    fixed once, at write) and rebases the window to positions 0 .. count - 1,
+    oldest slot first (delta = next_pos - count)."""
+    R, T, H, d = 10, 4, 2, 4
+    ring = WriteTimeRing(R, H, d)
+    rng = np.random.default_rng(1)
+    for w in range(5):
+        c = rng.standard_normal((T, H, d)).astype(np.float32) * (w + 1)
+        ring.write(c, 2 * c)
+    kam, vam, chunk = ring.kamax.copy(), ring.vamax.copy(), ring.chunk.copy()
+    assert ring.rebase() == 20 - 10
+    assert np.array_equal(ring.kamax, kam) and np.array_equal(ring.vamax, vam)
+    assert np.array_equal(ring.chunk, chunk)
+    assert list(_ring_logical(ring, ring.pos)) == list(range(10))
+    assert ring.next_pos == ring.count == 10 and ring.last_pos == 6
+
+
 def _ring_arrays(r: WriteTimeRing):
     return (r.k8, r.v8, r.kamax, r.vamax, r.pos, r.chunk)
 
