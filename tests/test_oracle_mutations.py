@@ -50,6 +50,29 @@ def _encode_truncating(x):
     return _ORIG_ENCODE(v)
 
 
+def _encode_nan_above_max(x):
+    # overflow to the NaN code instead of saturating at 448
+    x = np.asarray(x, np.float64)
+    out = _ORIG_ENCODE(np.clip(x, -448.0, 448.0))
+    return np.where(np.abs(x) > 448.0, np.where(np.signbit(x), 0xFF, 0x7F), out).astype(np.uint8)
+
+
+def _encode_ties_away(x):
+    # ties rounded away from zero instead of to the even code
+    x = np.asarray(x, np.float64)
+    a = np.abs(x)
+    _, E = np.frexp(np.where(a > 0, a, 1.0))
+    q = np.ldexp(1.0, np.maximum(E - 1, -6) - 3)
+    v = np.minimum(np.floor(a / q + 0.5) * q, 448.0) * np.where(np.signbit(x), -1.0, 1.0)
+    return _ORIG_ENCODE(v)
+
+
+def _encode_flush_subnormals(x):
+    # magnitudes below the smallest normal (2^-6) flushed to zero
+    x = np.asarray(x, np.float64)
+    return _ORIG_ENCODE(np.where(np.abs(x) < 2.0 ** -6, 0.0 * x, x))
+
+
 def _attention_no_scale(q, k, v):
     return _ORIG_ATT(np.asarray(q) * np.sqrt(np.asarray(q).shape[-1]), k, v)
 
@@ -195,6 +218,10 @@ CASES = [
     ("rotate-half pairing", [(rope_mod, "rotate", _rotate_halves)], t_rope.test_matches_complex_multiplication),
     ("frequency index", [(rope_mod, "freqs", _freqs_off_by_one)], t_rope.test_frequencies_closed_form),
     ("e4m3 truncation", [(e4m3_mod, "encode", _encode_truncating)], t_e4m3.test_encode_random_float32_matches_library),
+    ("e4m3 overflow to NaN", [(e4m3_mod, "encode", _encode_nan_above_max)], t_e4m3.test_satfinite),
+    ("e4m3 ties away from zero", [(e4m3_mod, "encode", _encode_ties_away)], t_e4m3.test_encode_at_rounding_midpoints),
+    ("e4m3 subnormals flushed", [(e4m3_mod, "encode", _encode_flush_subnormals)],
+     lambda: t_e4m3.test_encode_matches_library_cast_all_bf16(1.0)),
     ("missing 1/sqrt(d)", [(t_att, "attention_fp64", _attention_no_scale)], t_att.test_scale_is_one_over_sqrt_d),
     ("softmax axis", [(t_att, "attention_fp64", _attention_transposed)], t_att.test_rows_are_convex_combinations_and_key_order_free),
     ("K amax not pair norm", [(t_sch, "chunk_amax_k", _amax_plain)], t_sch.test_amax_k_is_largest_pair_norm_bruteforce),
