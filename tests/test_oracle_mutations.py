@@ -139,7 +139,7 @@ class _RewriteStaleScale(schemes_mod.WriteTimeRing):
         return slots
 
 
-def _rebase_planted(self, sign=-1, turn_v=False, rescale=False, shift_pos=True):
+def _rebase_planted(self, sign=-1, turn_v=False, rescale=False, shift_pos=True, shift_q=True):
     # the reset's steps (1-D) with one step made wrong
     delta = self.next_pos - self.count
     if delta != 0 and self.count > 0:
@@ -160,7 +160,8 @@ def _rebase_planted(self, sign=-1, turn_v=False, rescale=False, shift_pos=True):
         if shift_pos:
             self.pos[valid] -= delta
     self.next_pos = self.count
-    self.last_pos -= delta
+    if shift_q:
+        self.last_pos -= delta
     self.resets += 1
     return int(delta)
 
@@ -183,6 +184,11 @@ class _RebaseRescales(schemes_mod.WriteTimeRing):
 class _RebaseKeepsPositions(schemes_mod.WriteTimeRing):
     def rebase(self):
         return _rebase_planted(self, shift_pos=False)
+
+
+class _RebaseKeepsQPositions(schemes_mod.WriteTimeRing):
+    def rebase(self):
+        return _rebase_planted(self, shift_q=False)
 
 
 def _coords_swapped(p, S, W):
@@ -240,6 +246,8 @@ CASES = [
      t_ring.test_reset_keeps_scales_and_rebases_positions_to_the_window),
     ("rebase keeps positions", [(t_ring, "WriteTimeRing", _RebaseKeepsPositions)],
      t_ring.test_reset_keeps_scales_and_rebases_positions_to_the_window),
+    ("rebase leaves Q positions", [(t_sch, "WriteTimeRing", _RebaseKeepsQPositions)],
+     t_sch.test_attention_nearly_unchanged_by_a_reset),
 ]
 
 
