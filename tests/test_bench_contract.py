@@ -40,6 +40,11 @@ def test_workload_figures_and_the_3d_workload():
     import bench
     from kv_cache_gb300 import kvring as kv
     w = dict(bench.WORKLOAD)
+    # the pages' workload: every attention call reads 5,788 slots of which 757 are
+    # new, 240 calls per step (60 blocks x 4 passes), positions reset every 42
+    # steps (ai.info, "Characters funziona in tempo reale su quattro H100", section
+    # "La gestione della cache spostata al momento della scrittura")
+    assert (w["R"], w["T"], w["L"] * w["passes"], w["reset_every"]) == (5788, 757, 240, 42)
     write_bytes, attend_flop, rebase_bytes = bench.algorithmic(w)
     assert write_bytes == 757 * 16 * 128 * 6                # bf16 K, V in + e4m3 K, V out
     assert attend_flop == 4 * 757 * 5788 * 128 * 16          # Q K^T and P V, 2 FLOP per MAC
