@@ -18,7 +18,9 @@ A "step" is one pass of the whole hot path: [rebase when due] + 60 x write +
   bf16 peak x 2 (FP8); plus the write kernel against measured HBM bandwidth.
 * cpu_baseline / --impl reference: the CPU oracle (naive per-call upkeep, then
   float64 attention) timed on this host on a bounded sample (one block's
-  write + 4 attention calls), extrapolated to a 60-block step.
+  write + 4 attention calls), extrapolated to a 60-block step; its "upkeep"
+  object times the oracle's naive per-call upkeep against the write-time
+  ring's on one block (the CPU analogue of the pages' upkeep comparison).
 """
 from __future__ import annotations
 
@@ -373,6 +375,44 @@ def oracle_sample(cfg, seconds_hint=20.0):
                        f"at {H} heads x {d}, R={R}, T={T}; x{L} blocks (extrapolated)")
 
 
+def oracle_upkeep_sample(cfg):
+    """The CPU analogue of the pages' upkeep comparison, timed with the oracle on
+    one block: the naive scheme's per-step upkeep (a write that shifts the window,
+    then the whole window re-rotated and re-quantised before each of the P calls)
+    against the write-time ring's (RoPE and FP8 of the new chunk once, plus one
+    delta rotation of the ring every reset_every steps), both x L blocks."""
+    from kv_cache_gb300 import synthetic
+    from oracle.schemes import NaiveWindow, WriteTimeRing
+
+    L, H, d, R, T, P, RE = (cfg[k] for k in ("L", "H", "d", "R", "T", "passes", "reset_every"))
+    lay = cfg.get("rope_3d")
+    naive = NaiveWindow(R, H, d, layout=lay)
+    ring = WriteTimeRing(R, H, d, layout=lay)
+    f32 = synthetic.bf16_to_f32
+    fill = -(-R // T)
+    for w in range(fill):
+        k, v = f32(synthetic.chunk("k", w, T, H, d, True)), f32(synthetic.chunk("v", w, T, H, d, True))
+        naive.write(k, v)
+        ring.write(k, v)
+    k, v = f32(synthetic.chunk("k", fill, T, H, d, True)), f32(synthetic.chunk("v", fill, T, H, d, True))
+    t0 = time.perf_counter()
+    naive.write(k, v)
+    for _ in range(P):
+        naive.cache_codes()
+    t_naive = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    ring.write(k, v)
+    t_write = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    ring.rebase()
+    t_rebase = time.perf_counter() - t0
+    naive_ms = t_naive * L * 1e3
+    ring_ms = (t_write + t_rebase / RE) * L * 1e3
+    return {"naive_ms_per_step": naive_ms, "write_time_ms_per_step": ring_ms, "ratio": naive_ms / ring_ms,
+            "sample": f"one block: naive = 1 shifting write + {P} whole-window refreshes; write-time = 1 write "
+                      f"+ 1/{RE} of a full-ring rebase; x{L} blocks (extrapolated)"}
+
+
 # DRAM bytes (read + write) per attend_kernel launch, from the ncu capture summarised
 # in profiles/attend_kernel_production_ring_8_blocks.md; valid only for the attention
 # source it was taken on (sha256 prefix), else reported as null.
@@ -536,7 +576,7 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
                 "cpu_baseline": {"value": 1.0 / step_s, "unit": "steps/s", "cores": samples[0]["cores"],
                                  "cpu_model": samples[0]["cpu_model"], "kind": "oracle",
-                                 "sample": samples[0]["sample"]},
+                                 "sample": samples[0]["sample"], "upkeep": oracle_upkeep_sample(cfg)},
                 "e2e": {"value": 1.0 / step_s, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -589,7 +629,8 @@ def main():
     if not args.no_cpu_baseline:
         cb = oracle_sample(cfg)
         line["cpu_baseline"] = {"value": 1.0 / cb["step_s"], "unit": "steps/s", "cores": cb["cores"],
-                                "cpu_model": cb["cpu_model"], "kind": "oracle", "sample": cb["sample"]}
+                                "cpu_model": cb["cpu_model"], "kind": "oracle", "sample": cb["sample"],
+                                "upkeep": oracle_upkeep_sample(cfg)}
     print(json.dumps(line))
 
 

@@ -22,6 +22,8 @@ def test_reference_arm_prints_one_contract_line():
     assert j["value"] > 0 and j["unit"] == "steps/s" and j["higher_is_better"] is True
     assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["cores"] >= 1
     assert j["cpu_baseline"]["cpu_model"]
+    up = j["cpu_baseline"]["upkeep"]          # the CPU analogue of the pages' upkeep comparison
+    assert up["naive_ms_per_step"] > up["write_time_ms_per_step"] > 0
     assert j["e2e"] == {"value": j["value"], "unit": j["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert j["config"]["workload"].startswith("steady denoise step")
 
