@@ -61,3 +61,43 @@ def test_workload_figures_and_the_3d_workload():
     ring = kv.KVRing(1, c["H"], c["d"], c["R"], c["T"], max_position=c["R"] + 42 * c["T"], host_only=True,
                      rope_3d=c["rope_3d"])
     ring.close()
+
+
+def test_gpu_arm_line_has_every_contract_key(monkeypatch, capsys):
+    """The GPU arm's JSON line, assembled from a stand-in for the timed run (no GPU
+    here): every key of the contract, with the roofline and CPU-baseline objects."""
+    sys.path.insert(0, ROOT)
+    import bench
+    K = 42
+    fake = dict(ms=15.4 * K, w_ms=[0.0166] * 60, a_ms=[0.0631] * 240, r_ms=[], rb_ms=0.275, launches=25201,
+                clocks={"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 4},
+                e2e_ms=16.1 * 12, e2e_steps=12, h2d=1116241920, d2h=24805376)
+    monkeypatch.setattr(bench, "run_gpu", lambda args, cfg, rank, world: fake)
+    monkeypatch.setattr(bench, "oracle_sample", lambda cfg: {"block_s": 6.6, "step_s": 397.0, "cores": 16,
+                                                             "cpu_model": "host", "sample": "one block"})
+    monkeypatch.setattr(bench, "oracle_upkeep_sample", lambda cfg: {"naive_ms_per_step": 6.8e5,
+                                                                    "write_time_ms_per_step": 2.0e4, "ratio": 34.0,
+                                                                    "sample": "one block"})
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    monkeypatch.delenv("RANK", raising=False)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    bench.main()
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    j = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "e2e", "gpu_launches", "roofline",
+                "cpu_baseline", "clocks"):
+        assert key in j, key
+    assert j["n_gpus"] == 1 and j["steps"] == K and abs(j["ms_per_step"] - 15.4) < 1e-9
+    assert abs(j["value"] - 1e3 / 15.4) < 1e-6 and j["unit"] == "steps/s" and j["scaling"] == "weak"
+    assert j["config"]["workload"].startswith("steady denoise step") and "l2" in j["config"]
+    assert abs(j["e2e"]["value"] - 1e3 / 16.1) < 1e-6
+    assert j["e2e"]["h2d_bytes_per_step"] > 0 and j["e2e"]["d2h_bytes_per_step"] > 0
+    rf = j["roofline"]
+    assert rf["bound"] == "tensor" and rf["unit"] == "TFLOP/s"
+    assert abs(rf["achieved"] - 4 * 757 * 5788 * 128 * 16 / 63.1e-6 / 1e12) < 1e-6
+    assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-12
+    cb = j["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 16 and cb["upkeep"]["ratio"] == 34.0
+    assert j["clocks"]["sm_mhz"] == 2070.0
