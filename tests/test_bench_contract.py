@@ -101,3 +101,19 @@ def test_gpu_arm_line_has_every_contract_key(monkeypatch, capsys):
     cb = j["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] == 16 and cb["upkeep"]["ratio"] == 34.0
     assert j["clocks"]["sm_mhz"] == 2070.0
+
+
+def test_rebase_stress_line_counts_only_the_bytes_a_reset_moves(monkeypatch, capsys):
+    """--rebase-stress (1-D and 3-D): the roofline's algorithmic bytes are the K
+    bytes a reset reads and writes -- whole rows in 1-D, the time-band pieces in 3-D."""
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setattr(bench, "run_rebase_stress", lambda args, cfg: [0.25] * 10)
+    for extra, R, row in (([], 5788, 128), (["--rope-3d"], 5797, 48)):
+        monkeypatch.setattr(sys, "argv", ["bench.py", "--rebase-stress"] + extra)
+        bench.main()
+        j = json.loads([l for l in capsys.readouterr().out.splitlines() if l.startswith("{")][0])
+        nbytes = 2.0 * 60 * 16 * R * row
+        assert j["value"] == 0.25 and j["higher_is_better"] is False
+        assert abs(j["roofline"]["achieved"] - nbytes / 0.25e-3 / 1e9) < 1e-6
+        assert ("3-D" in j["config"]["workload"]) == bool(extra)
