@@ -12,15 +12,26 @@ A "step" is one pass of the whole hot path: [rebase when due] + 60 x write +
 * value: steps/s over all ranks (replicas: each rank runs the full workload on
   its own GPU; no data-path collective), inputs resident in HBM.
 * e2e: the same steps with each step's K, V, Q copied host->device from pinned
-  memory and every attention output copied back, inside the timed region.
+  memory and all 240 attention outputs (one buffer per layer and pass) copied
+  back to pinned host memory, inside the timed region.
+* The timed steps start at a reset step (positions reset before that step's
+  writes), so K timed steps hold ceil(K / 42) rebases: at least the reset's
+  share of the path, never less.
 * roofline: the attention call (Q-prep + attention + split combine launches),
   algorithmic FLOP 4*T*R*d*H per call at a full ring, against the measured
   bf16 peak x 2 (FP8); plus the write kernel against measured HBM bandwidth.
 * cpu_baseline / --impl reference: the CPU oracle (naive per-call upkeep, then
-  float64 attention) timed on this host on a bounded sample (one block's
-  write + 4 attention calls), extrapolated to a 60-block step; its "upkeep"
-  object times the oracle's naive per-call upkeep against the write-time
-  ring's on one block (the CPU analogue of the pages' upkeep comparison).
+  float64 attention) timed on this host.  A full step is hours of CPU work, so
+  one timed "step" of the reference arm is one block's step (1 write + 4
+  attention calls) and the step time is that x 60 blocks, marked extrapolated;
+  the line's `steps` counts the full steps actually timed (block steps / 60).
+  The tiny configuration (100 steps) and one production write + attention are
+  timed whole, beside the GPU's time for the same work.  `upkeep` times the
+  oracle's naive per-call upkeep against the write-time ring's on one block (the
+  CPU analogue of the pages' upkeep comparison).
+* --session: the unsharded-width session (60 blocks x 64 heads, 1,000 steps,
+  resets every 42): per-step times (median, p99) and the drift against the
+  oracle at steps 1, 41, 42, 43, 500 and 999.
 """
 from __future__ import annotations
 
@@ -42,6 +53,8 @@ if ROOT not in sys.path:
 METRIC = "cache upkeep ms/step & GB/s; FP8 attn TFLOP/s (757q×5788kv); % of GB300 roofline"
 WORKLOAD = dict(name="steady denoise step: 60 blocks x (1 write + 4 attention calls), reset every 42 steps",
                 L=60, H=16, d=128, R=5788, T=757, passes=4, reset_every=42)
+TINY = dict(name="tiny: 1 block, 2 heads x 64, 96 slots, 32-token writes, 4 attention calls per step, 100 steps, "
+                 "resets every 42", L=1, H=2, d=64, R=96, T=32, passes=4, reset_every=42, steps=100)
 SMALL = dict(name="small check: 4 blocks x (1 write + 4 attention calls)", L=4, H=16, d=128, R=5788, T=757,
              passes=4, reset_every=42)
 # 3-D (time, height, width) video RoPE: frames of 11 x 17 latent tokens, writes of 4
@@ -136,7 +149,8 @@ def run_gpu(args, cfg, rank, world):
     ring = kv.KVRing(L, H, d, R, T, max_position=R + RE * T, naive_upkeep=NV, rope_3d=cfg.get("rope_3d"))
     host, pool = make_pool(cfg, torch, device)
     stream = torch.cuda.current_stream(device)
-    outs = [torch.empty((T, H, d), dtype=torch.float32, device=device) for _ in range(P)]
+    # one output buffer per (layer, pass), as a model keeps each block's attention output
+    outs = [torch.empty((T, H, d), dtype=torch.float32, device=device) for _ in range(L * P)]
 
     step_counter = [0]
 
@@ -150,6 +164,7 @@ def run_gpu(args, cfg, rank, world):
             if timers is not None:
                 timers["rebase"][1].record(stream)
                 timers["n_rebase"] += 1
+        ob = out_bufs or outs
         for p in range(P):
             for l in range(L):
                 if p < WP:
@@ -178,10 +193,16 @@ def run_gpu(args, cfg, rank, world):
                 if timers is not None:
                     ev = timers["attend"][timers["na"]]
                     ev[0].record(stream)
-                ring.attend(l, q, (out_bufs or outs)[p], stream=stream)
+                ring.attend(l, q, ob[p * L + l], stream=stream)
                 if timers is not None:
                     ev[1].record(stream)
                     timers["na"] += 1
+
+    def to_reset_step():
+        """Untimed steps until the next step is a reset step (so a timed run of K
+        steps holds ceil(K / RE) rebases, the first in its first step)."""
+        while step_counter[0] % RE != 0:
+            one_step()
 
     # fill the rings (untimed): 8 writes reach the steady state (count = R)
     fill = -(-R // T)
@@ -189,6 +210,7 @@ def run_gpu(args, cfg, rank, world):
         one_step()
     for _ in range(args.warmup):
         one_step()
+    to_reset_step()
     torch.cuda.synchronize(device)
     ring.check_device(stream)
 
@@ -198,6 +220,7 @@ def run_gpu(args, cfg, rank, world):
               "rebase": (mk(), mk()), "nw": 0, "na": 0, "n_rebase": 0,
               "refresh": [(mk(), mk()) for _ in range(K * L * P if NV else 0)], "nr": 0}
     launches0 = ring.launch_count()
+    first_timed = step_counter[0]
     sampler = ClockSampler(device.index)
     if world > 1:
         import torch.distributed as dist
@@ -214,12 +237,14 @@ def run_gpu(args, cfg, rank, world):
     if world > 1:
         dist.barrier()
     launches = ring.launch_count() - launches0
+    resets_timed = sum(1 for st in range(first_timed, first_timed + K) if st > 0 and st % RE == 0)
     if ring.check_device(stream) != kv.KVRING_OK:
         raise RuntimeError("device wait timed out during the timed region: " + kv.kvring_last_error(ring.handle))
     ms = t0.elapsed_time(t1)
-    # per-call breakdown: the same number of steps again, with an event pair around
-    # each call (events between calls keep consecutive kernels from overlapping, so
-    # these are taken apart from the step time above; K >= reset_every includes a reset)
+    # per-call breakdown: the same number of steps again, from a reset step, with an
+    # event pair around each call (events between calls keep consecutive kernels
+    # from overlapping, so these are taken apart from the step time above)
+    to_reset_step()
     for _ in range(K):
         one_step(timers)
     torch.cuda.synchronize(device)
@@ -229,10 +254,11 @@ def run_gpu(args, cfg, rank, world):
     a_ms = [a.elapsed_time(b) for a, b in timers["attend"][:timers["na"]]]
     r_ms = [a.elapsed_time(b) for a, b in timers["refresh"][:timers["nr"]]]
     rb_ms = timers["rebase"][0].elapsed_time(timers["rebase"][1]) if timers["n_rebase"] else None
+    del timers
 
-    # ---- end to end: host inputs (pinned) -> device, attention outputs -> host, every step.
+    # ---- end to end: host inputs (pinned) -> device, all attention outputs -> host, every step.
     # Two buffer sets: a copy stream brings step s + 1's K, V and Q in while step s
-    # computes, and reads step s's outputs back once it has finished (the way a
+    # computes, and reads step s's 240 outputs back once it has finished (the way a
     # serving loop overlaps its transfers); every step's copies are inside the
     # timed region.
     e2e_steps = max(1, min(K, args.e2e_steps))
@@ -242,12 +268,14 @@ def run_gpu(args, cfg, rank, world):
                "v": [torch.empty((T, H, d), dtype=torch.bfloat16, device=device) for _ in range(L * WP)],
                "q": [torch.empty((T, H, d), dtype=torch.bfloat16, device=device) for _ in range(L * P)]}
               for _ in range(NB)]
-    dev_out = [[torch.empty((T, H, d), dtype=torch.float32, device=device) for _ in range(P)] for _ in range(NB)]
-    host_out = [[torch.empty((T, H, d), dtype=torch.float32).pin_memory() for _ in range(P)] for _ in range(NB)]
+    dev_out = [outs] + [[torch.empty((T, H, d), dtype=torch.float32, device=device) for _ in range(L * P)]
+                        for _ in range(NB - 1)]
+    host_out = [[torch.empty((T, H, d), dtype=torch.float32).pin_memory() for _ in range(L * P)] for _ in range(NB)]
     cs = torch.cuda.Stream(device)
     ev = lambda: torch.cuda.Event()
     in_ready, comp_done, out_read = [ev() for _ in range(NB)], [ev() for _ in range(NB)], [ev() for _ in range(NB)]
     h2d = d2h = 0
+    to_reset_step()
     s0 = step_counter[0]
 
     def issue_inputs(n):
@@ -282,10 +310,10 @@ def run_gpu(args, cfg, rank, world):
         comp_done[b].record(stream)
         with torch.cuda.stream(cs):
             cs.wait_event(comp_done[b])
-            for p in range(P):
-                host_out[b][p].copy_(dev_out[b][p], non_blocking=True)
+            for i in range(L * P):
+                host_out[b][i].copy_(dev_out[b][i], non_blocking=True)
             out_read[b].record(cs)
-        d2h += P * T * H * d * 4
+        d2h += L * P * T * H * d * 4
     fin = ev()
     fin.record(cs)
     stream.wait_event(fin)
@@ -293,8 +321,245 @@ def run_gpu(args, cfg, rank, world):
     torch.cuda.synchronize(device)
     e2e_ms = e0.elapsed_time(e1)
     ring.close()
+    del dev_in, dev_out, host_out, pin
     return dict(ms=ms, w_ms=w_ms, a_ms=a_ms, r_ms=r_ms, rb_ms=rb_ms, launches=launches, clocks=clocks,
-                e2e_ms=e2e_ms, e2e_steps=e2e_steps, h2d=h2d // e2e_steps, d2h=d2h // e2e_steps)
+                e2e_ms=e2e_ms, e2e_steps=e2e_steps, h2d=h2d // e2e_steps, d2h=d2h // e2e_steps,
+                resets_timed=resets_timed)
+
+
+def run_whole_configs_gpu(torch_device_index=0, reps=20):
+    """GPU time of the two configurations the CPU oracle is also timed on whole:
+    the tiny case (1 block, 2 heads x 64, 96 slots, 32-token writes, 4 attention
+    calls per step, 100 steps with resets every 42) and one production write +
+    one 757-query attention call on a full 5,788-slot ring of 16 heads x 128."""
+    import torch
+    from kv_cache_gb300 import kvring as kv
+    from kv_cache_gb300 import synthetic
+    device = torch.device("cuda", torch_device_index)
+    stream = torch.cuda.current_stream(device)
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    dev = lambda bits: torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(device)
+    out = {}
+    # tiny: 100 steps, whole
+    tc = TINY
+    ring = kv.KVRing(1, tc["H"], tc["d"], tc["R"], tc["T"], max_position=tc["R"] + 42 * tc["T"])
+    kin = [dev(synthetic.chunk("k", i, tc["T"], tc["H"], tc["d"])) for i in range(synthetic.POOL)]
+    vin = [dev(synthetic.chunk("v", i, tc["T"], tc["H"], tc["d"])) for i in range(synthetic.POOL)]
+    qin = [dev(synthetic.chunk("q", i, tc["T"], tc["H"], tc["d"])) for i in range(synthetic.POOL)]
+    o = torch.empty((tc["T"], tc["H"], tc["d"]), dtype=torch.float32, device=device)
+
+    def tiny_run():
+        for s in range(tc["steps"]):
+            if s > 0 and s % 42 == 0:
+                ring.rebase(stream)
+            ring.write(0, kin[s % 16], vin[s % 16], stream=stream)
+            for p in range(tc["passes"]):
+                ring.attend(0, qin[(s + p) % 16], o, stream=stream)
+
+    tiny_run()        # warm-up (a fresh ring each time would re-create it; the schedule repeats)
+    ring.close()
+    ring = kv.KVRing(1, tc["H"], tc["d"], tc["R"], tc["T"], max_position=tc["R"] + 42 * tc["T"])
+    torch.cuda.synchronize(device)
+    e0, e1 = mk(), mk()
+    e0.record(stream)
+    tiny_run()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    out["tiny_100_steps_ms"] = e0.elapsed_time(e1)
+    ring.close()
+    # one production write + one attention call on a full ring
+    c = WORKLOAD
+    ring = kv.KVRing(1, c["H"], c["d"], c["R"], c["T"], max_position=c["R"] + 42 * c["T"])
+    kin = [dev(synthetic.chunk("k", i, c["T"], c["H"], c["d"], True)) for i in range(4)]
+    vin = [dev(synthetic.chunk("v", i, c["T"], c["H"], c["d"], True)) for i in range(4)]
+    qin = dev(synthetic.chunk("q", 0, c["T"], c["H"], c["d"], True))
+    o = torch.empty((c["T"], c["H"], c["d"]), dtype=torch.float32, device=device)
+    for w in range(-(-c["R"] // c["T"])):
+        ring.write(0, kin[w % 4], vin[w % 4], stream=stream)
+    ts = []
+    for r in range(reps + 3):
+        e0, e1 = mk(), mk()
+        e0.record(stream)
+        ring.write(0, kin[r % 4], vin[r % 4], stream=stream)
+        ring.attend(0, qin, o, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        if r >= 3:
+            ts.append(e0.elapsed_time(e1))
+    out["single_layer_write_attend_ms"] = statistics.median(ts)
+    if ring.check_device(stream) != kv.KVRING_OK:
+        raise RuntimeError(kv.kvring_last_error(ring.handle))
+    ring.close()
+    return out
+
+
+SESSION = dict(name="unsharded-width session: 60 blocks of 64 heads x (1 write + 4 attention calls), 1,000 steps, "
+                    "resets every 42", L=60, H=64, d=128, R=5788, T=757, passes=4, reset_every=42, steps=1000,
+               checks=(1, 41, 42, 43, 500, 999), replay=10)
+
+
+def run_session(args, cfg):
+    """The unsharded-width session: every step is [rebase when due] + L writes + 4L
+    attention calls, each step timed with its own event pair.  At the check steps
+    the cache of the first and last block is compared with an oracle ring whose
+    bookkeeping comes from a bookkeeping-only oracle ring (1 head, d = 2, every
+    step) and which replays the last `replay` steps with data (the ring holds the
+    chunks of the last 8 steps, and a reset inside the replayed steps turns only
+    chunks written inside them), and the step's last attention call of those
+    blocks is compared on 4 heads x 64 query rows."""
+    import copy
+    from collections import deque
+
+    import torch
+    from kv_cache_gb300 import kvring as kv
+    from kv_cache_gb300 import synthetic
+    from oracle import e4m3
+    from oracle.schemes import WriteTimeRing
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    L, H, d, R, T, P, RE = (cfg[k] for k in ("L", "H", "d", "R", "T", "passes", "reset_every"))
+    steps, checks, replay = cfg["steps"], [c for c in cfg["checks"] if c < cfg["steps"]], cfg["replay"]
+    ring = kv.KVRing(L, H, d, R, T, max_position=R + RE * T)
+    host, pool = make_pool(cfg, torch, device)
+    f32 = synthetic.bf16_to_f32
+    stream = torch.cuda.current_stream(device)
+    outs = [torch.empty((T, H, d), dtype=torch.float32, device=device) for _ in range(L * P)]
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+
+    def one_step(s, timers=None):
+        if s > 0 and s % RE == 0:
+            if timers:
+                timers["rebase"][0].record(stream)
+            ring.rebase(stream)
+            if timers:
+                timers["rebase"][1].record(stream)
+        for p in range(P):
+            for l in range(L):
+                if p == 0:
+                    i = synthetic.pool_index(s, l, 4, L)
+                    if timers:
+                        timers["write"].append((mk(), mk()))
+                        timers["write"][-1][0].record(stream)
+                    ring.write(l, pool["k"][i], pool["v"][i], stream=stream)
+                    if timers:
+                        timers["write"][-1][1].record(stream)
+                if timers:
+                    timers["attend"].append((mk(), mk()))
+                    timers["attend"][-1][0].record(stream)
+                ring.attend(l, pool["q"][synthetic.pool_index(s, l, p, L)], outs[p * L + l], stream=stream)
+                if timers:
+                    timers["attend"][-1][1].record(stream)
+
+    tiny = WriteTimeRing(R, 1, 2)
+    z = np.zeros((T, 1, 2), np.float32)
+    before = deque(maxlen=replay)
+    rng = np.random.default_rng(21)
+    heads = np.array([0, 21, 42, 63])
+    rows = np.unique(np.concatenate([rng.choice(T, 60, replace=False), [0, 255, 256, 756]]))
+    ev = [(mk(), mk()) for _ in range(steps)]
+    drift = []
+    sampler = ClockSampler(0)
+    sampler.start()
+    for s in range(steps):
+        before.append(copy.deepcopy(tiny))
+        if s > 0 and s % RE == 0:
+            tiny.rebase()
+        tiny.write(z, z)
+        ev[s][0].record(stream)
+        one_step(s)
+        ev[s][1].record(stream)
+        if s not in checks:
+            continue
+        torch.cuda.synchronize(device)
+        if ring.check_device(stream) != kv.KVRING_OK:
+            raise RuntimeError("device wait timed out in the session: " + kv.kvring_last_error(ring.handle))
+        first = s - len(before) + 1
+        for l in (0, L - 1):
+            o = WriteTimeRing(R, H, d)
+            for f in ("head", "count", "next_pos", "writes", "resets", "last_pos", "last_n"):
+                setattr(o, f, getattr(before[0], f))
+            o.pos, o.chunk = before[0].pos.copy(), before[0].chunk.copy()
+            for t in range(first, s + 1):
+                if t > 0 and t % RE == 0:
+                    o.rebase()
+                i = synthetic.pool_index(t, l, 4, L)
+                o.write(f32(host["k"][i]), f32(host["v"][i]))
+            snap = ring.snapshot(l, stream)
+            valid = o.pos >= 0
+            st = ring.state(l)
+            book = (st["head"], st["count"], st["next_pos"], st["writes"]) == (o.head, o.count, o.next_pos, o.writes)
+            book = book and bool(np.array_equal(snap["pos"].astype(np.int64), o.pos))
+            gk, gv = snap["k"][:, valid], snap["v"][:, valid]
+            rk, rv = o.k8[:, valid], o.v8[:, valid]
+            kstep = float(np.max(np.abs(e4m3.decode(gk) - e4m3.decode(rk)) /
+                                 e4m3.ulp_at(np.maximum(np.abs(e4m3.decode(gk)), np.abs(e4m3.decode(rk))))))
+            qi = synthetic.pool_index(s, l, P - 1, L)
+            got = outs[(P - 1) * L + l].cpu().numpy()[np.ix_(rows, heads)].astype(np.float64)
+            ref = o.attend(f32(host["q"][qi]), heads=heads, rows=rows)
+            drift.append({"step": s, "block": l, "bookkeeping_exact": book,
+                          "k_identical": float(np.mean(gk == rk)), "v_identical": float(np.mean(gv == rv)),
+                          "k_max_steps": kstep, "attn_max_abs": float(np.max(np.abs(got - ref))),
+                          "attn_mean_rel": float(np.sum(np.abs(got - ref)) / np.sum(np.abs(ref)))})
+    torch.cuda.synchronize(device)
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    # per-call breakdown from a reset step, RE steps with an event pair around each call
+    s = steps
+    while s % RE:
+        one_step(s)
+        s += 1
+    timers = {"write": [], "attend": [], "rebase": (mk(), mk())}
+    for k in range(RE):
+        one_step(s + k, timers)
+    torch.cuda.synchronize(device)
+    if ring.check_device(stream) != kv.KVRING_OK:
+        raise RuntimeError(kv.kvring_last_error(ring.handle))
+    w = [a.elapsed_time(b) for a, b in timers["write"]]
+    a = [a_.elapsed_time(b) for a_, b in timers["attend"]]
+    rb = timers["rebase"][0].elapsed_time(timers["rebase"][1])
+    ring.close()
+    return dict(step_ms=step_ms, drift=drift, clocks=clocks, w_ms=w, a_ms=a, rb_ms=rb)
+
+
+def session_line(r, cfg, peaks, peak_src):
+    L, H, d, R, T, P = (cfg[k] for k in ("L", "H", "d", "R", "T", "passes"))
+    write_bytes, attend_flop, rebase_bytes = algorithmic(cfg)
+    st = sorted(r["step_ms"])
+    med = statistics.median(st)
+    p99 = st[min(len(st) - 1, int(round(0.99 * (len(st) - 1))))]
+    total = sum(r["step_ms"])
+    w_avg, a_avg = statistics.mean(r["w_ms"]), statistics.mean(r["a_ms"])
+    fp8 = 2.0 * peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    first = [x for x in r["drift"] if x["step"] == min(x["step"] for x in r["drift"])]
+    last = [x for x in r["drift"] if x["step"] == max(x["step"] for x in r["drift"])]
+    band = max(x["attn_max_abs"] for x in first)
+    band_rel = max(x["attn_mean_rel"] for x in first)
+    codes_exact = all(x["k_identical"] == 1.0 and x["v_identical"] == 1.0 and x["bookkeeping_exact"]
+                      for x in r["drift"])
+    return {
+        "metric": "sustained ms/step over the session, and drift against the oracle", "value": total / len(st),
+        "unit": "ms/step", "higher_is_better": False, "n_gpus": 1, "steps": len(st), "dtype": "fp8_e4m3",
+        "data": "synthetic",
+        "config": {"workload": cfg["name"], "blocks": L, "heads": H, "head_dim": d, "ring_slots": R,
+                   "tokens_per_write": T, "attention_calls_per_step": L * P,
+                   "l2": f"inputs larger than L2: {2 * L * H * R * d / 1e9:.2f} GB of e4m3 rings read per step"},
+        "step_ms": {"mean": total / len(st), "median": med, "p99": p99, "max": st[-1], "min": st[0]},
+        "breakdown": {"upkeep_ms_per_step": w_avg * L, "write_us_per_call": w_avg * 1e3,
+                      "write_gbs": write_bytes / (w_avg * 1e-3) / 1e9,
+                      "attend_us_per_call": a_avg * 1e3, "attend_ms_per_step": a_avg * L * P,
+                      "attend_tflops_per_call": attend_flop / (a_avg * 1e-3) / 1e12,
+                      "attend_frac_fp8": attend_flop / (a_avg * 1e-3) / 1e12 / fp8,
+                      "rebase_ms": r["rb_ms"], "rebase_gbs": rebase_bytes / (r["rb_ms"] * 1e-3) / 1e9,
+                      "rebase_frac_hbm": rebase_bytes / (r["rb_ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                      "peaks": f"{peak_src}: HBM {peaks['hbm_gbs']} GB/s, FP8 2 x bf16 sustained"},
+        "drift": r["drift"],
+        "no_drift": bool(codes_exact and all(x["attn_max_abs"] <= max(2 * band, 1e-3) and
+                                             x["attn_mean_rel"] <= max(2 * band_rel, 1e-4) for x in last)),
+        "drift_rule": "cache bytes and bookkeeping identical to the oracle at every check; attention errors at the "
+                      "last check within twice those at the first",
+        "clocks": r["clocks"],
+    }
 
 
 def run_rebase_stress(args, cfg, rounds=10):
@@ -345,8 +610,11 @@ def cpu_model():
     return platform.processor() or platform.machine()
 
 
-def oracle_sample(cfg, seconds_hint=20.0):
-    """Time the CPU oracle on one block: a full window of writes, then one step's write + 4 calls."""
+def oracle_sample(cfg, n=1, warm=0):
+    """Time the CPU oracle on one block: a full window of writes (untimed), then
+    `warm` untimed and `n` timed block steps, each one write + 4 attention calls
+    (naive per-call upkeep, float64 attention).  Returns the per-block-step
+    times and the full-step figure extrapolated to all blocks."""
     from kv_cache_gb300 import synthetic
     from oracle.schemes import NaiveWindow
 
@@ -357,22 +625,64 @@ def oracle_sample(cfg, seconds_hint=20.0):
     for w in range(fill):
         naive.write(f32(synthetic.chunk("k", w, T, H, d, True)), f32(synthetic.chunk("v", w, T, H, d, True)))
     qs = [f32(synthetic.chunk("q", p, T, H, d, True)) for p in range(P)]
-    k = f32(synthetic.chunk("k", fill, T, H, d, True))
-    v = f32(synthetic.chunk("v", fill, T, H, d, True))
     WP = cfg.get("writes_per_step", 1)
+    times = []
+    for i in range(warm + n):
+        k = f32(synthetic.chunk("k", fill + i, T, H, d, True))
+        v = f32(synthetic.chunk("v", fill + i, T, H, d, True))
+        t0 = time.perf_counter()
+        naive.write(k, v)
+        for p in range(P):
+            if 0 < p < WP:
+                naive.rewrite(k, v)
+            naive.attend(qs[p])
+        if i >= warm:
+            times.append(time.perf_counter() - t0)
+    block_s = statistics.median(times)
+    threads = os.cpu_count()
+    return dict(block_s=block_s, block_times_s=times, step_s=block_s * L, cores=threads, cpu_model=cpu_model(),
+                sample=f"{n} block step(s) (1 write + {WP - 1} rewrites + {P} attention calls each, naive per-call "
+                       f"upkeep, float64 attention{', 3-D RoPE' if cfg.get('rope_3d') else ''}) at {H} heads x {d}, "
+                       f"R={R}, T={T}; full step = median block step x {L} blocks (extrapolated)")
+
+
+def oracle_whole_configs():
+    """The CPU oracle timed whole on the two small configurations: the tiny case
+    (100 steps: write, 4 naive attention calls, resets every 42) and one
+    production write + one attention call on a full 16-head ring."""
+    from kv_cache_gb300 import synthetic
+    from oracle.schemes import NaiveWindow
+
+    f32 = synthetic.bf16_to_f32
+    tc = TINY
+    naive = NaiveWindow(tc["R"], tc["H"], tc["d"])
+    kin = [f32(synthetic.chunk("k", i, tc["T"], tc["H"], tc["d"])) for i in range(synthetic.POOL)]
+    vin = [f32(synthetic.chunk("v", i, tc["T"], tc["H"], tc["d"])) for i in range(synthetic.POOL)]
+    qin = [f32(synthetic.chunk("q", i, tc["T"], tc["H"], tc["d"])) for i in range(synthetic.POOL)]
+    t0 = time.perf_counter()
+    for s in range(tc["steps"]):
+        if s > 0 and s % tc["reset_every"] == 0:
+            naive.rebase()
+        naive.write(kin[s % 16], vin[s % 16])
+        for p in range(tc["passes"]):
+            naive.attend(qin[(s + p) % 16])
+    tiny_s = time.perf_counter() - t0
+    c = WORKLOAD
+    naive = NaiveWindow(c["R"], c["H"], c["d"])
+    for w in range(-(-c["R"] // c["T"])):
+        naive.write(f32(synthetic.chunk("k", w % 4, c["T"], c["H"], c["d"], True)),
+                    f32(synthetic.chunk("v", w % 4, c["T"], c["H"], c["d"], True)))
+    k = f32(synthetic.chunk("k", 1, c["T"], c["H"], c["d"], True))
+    v = f32(synthetic.chunk("v", 1, c["T"], c["H"], c["d"], True))
+    q = f32(synthetic.chunk("q", 0, c["T"], c["H"], c["d"], True))
     t0 = time.perf_counter()
     naive.write(k, v)
-    for p in range(P):
-        if 0 < p < WP:
-            naive.rewrite(k, v)
-        naive.attend(qs[p])
-    block_s = time.perf_counter() - t0
-    step_s = block_s * L
-    threads = os.cpu_count()
-    return dict(block_s=block_s, step_s=step_s, cores=threads, cpu_model=cpu_model(),
-                sample=f"one block (1 write + {WP - 1} rewrites + {P} attention calls, naive per-call upkeep, "
-                       f"float64 attention{', 3-D RoPE' if cfg.get('rope_3d') else ''}) "
-                       f"at {H} heads x {d}, R={R}, T={T}; x{L} blocks (extrapolated)")
+    naive.attend(q)
+    single_s = time.perf_counter() - t0
+    return {"tiny_100_steps_ms": tiny_s * 1e3, "single_layer_write_attend_ms": single_s * 1e3,
+            "tiny_workload": tc["name"],
+            "single_layer_workload": "one write of 757 tokens + one 757-query attention call, full 5,788-slot "
+                                     "ring of 16 heads x 128 (naive per-call upkeep, float64 attention)"}
 
 
 def oracle_upkeep_sample(cfg):
@@ -508,6 +818,10 @@ def main():
                     help="number of blocks (profiling cases; 8 blocks already keep one layer's ring out of L2 "
                          "between its visits)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--session", action="store_true",
+                    help="the unsharded-width session: 60 blocks x 64 heads, 1,000 steps, resets every 42; "
+                         "per-step times and drift against the oracle (one JSON line)")
+    ap.add_argument("--session-steps", type=int, default=0, help="steps of --session (default 1,000)")
     ap.add_argument("--naive-upkeep", action="store_true",
                     help="the comparison scheme: shift the bf16 window on write, re-rotate and re-quantise "
                          "all of it before every attention call (kvring_naive_refresh)")
@@ -529,6 +843,17 @@ def main():
         cfg["L"] = args.blocks
     if args.probe_peaks:
         print(json.dumps(probe_peaks()))
+        return
+    if args.session:
+        scfg = dict(SESSION)
+        if args.session_steps > 0:
+            scfg["steps"] = args.session_steps
+            scfg["name"] = scfg["name"].replace("1,000 steps", f"{args.session_steps} steps")
+        if args.blocks > 0:
+            scfg["name"] = scfg["name"].replace("60 blocks", f"{args.blocks} blocks")
+            scfg["L"] = args.blocks
+        peaks, peak_src = load_peaks()
+        print(json.dumps(session_line(run_session(args, scfg), scfg, peaks, peak_src)))
         return
     if args.rebase_stress:
         ts = run_rebase_stress(args, cfg)
@@ -564,19 +889,25 @@ def main():
               "l2": (f"inputs larger than L2: {2 * L * H * R * d / 1e9:.2f} GB of e4m3 rings read per step"
                      if 2 * L * H * R * d > 129e6 else
                      f"check run, not a bench number: {2 * L * H * R * d / 1e9:.2f} GB of rings fit in L2"),
-              "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+              "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+              "timed_steps": "start at a reset step, so K timed steps hold ceil(K / 42) rebases"}
 
     if args.impl == "reference":
         if rank != 0:
             return
-        samples = [oracle_sample(cfg) for _ in range(max(1, args.steps if args.steps < 3 else 1))]
-        step_s = statistics.median(s["step_s"] for s in samples)
+        # each timed "step" is one block's step; the full step is extrapolated x L
+        n = max(1, args.steps)
+        cb = oracle_sample(cfg, n=n, warm=min(args.warmup, 1))
+        step_s = cb["step_s"]
         line = {"impl": "reference", "metric": METRIC, "value": 1.0 / step_s, "unit": "steps/s", "n_gpus": 0,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
-                "cpu_baseline": {"value": 1.0 / step_s, "unit": "steps/s", "cores": samples[0]["cores"],
-                                 "cpu_model": samples[0]["cpu_model"], "kind": "oracle",
-                                 "sample": samples[0]["sample"], "upkeep": oracle_upkeep_sample(cfg)},
+                "steps": n / L, "block_steps_timed": n, "warmup": min(args.warmup, 1),
+                "ms_per_step": step_s * 1e3, "extrapolated": True, "extrapolation_factor": L,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": 1.0 / step_s, "unit": "steps/s", "cores": cb["cores"],
+                                 "cpu_model": cb["cpu_model"], "kind": "oracle", "sample": cb["sample"],
+                                 "block_step_ms": [t * 1e3 for t in cb["block_times_s"]],
+                                 "upkeep": oracle_upkeep_sample(cfg), "whole": oracle_whole_configs()},
                 "e2e": {"value": 1.0 / step_s, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -605,6 +936,7 @@ def main():
         "e2e": {"value": world * 1e3 / e2e_per, "unit": "steps/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"], "steps": r["e2e_steps"]},
         "gpu_launches": r["launches"],
+        "resets_in_timed_steps": r["resets_timed"],
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": fp8_sustained, "unit": "TFLOP/s",
                      "frac": attn_tflops / fp8_sustained, "traffic": attend_traffic(cfg),
                      "traffic_unit": "bytes per attend_kernel launch (ncu, 8-block run)",
@@ -628,9 +960,15 @@ def main():
     }
     if not args.no_cpu_baseline:
         cb = oracle_sample(cfg)
+        whole_cpu = oracle_whole_configs()
+        whole_gpu = run_whole_configs_gpu()
         line["cpu_baseline"] = {"value": 1.0 / cb["step_s"], "unit": "steps/s", "cores": cb["cores"],
                                 "cpu_model": cb["cpu_model"], "kind": "oracle", "sample": cb["sample"],
-                                "upkeep": oracle_upkeep_sample(cfg)}
+                                "upkeep": oracle_upkeep_sample(cfg),
+                                "whole": {k: {"cpu_ms": whole_cpu[k], "gpu_ms": whole_gpu[k],
+                                              "workload": whole_cpu["tiny_workload" if k.startswith("tiny")
+                                                                    else "single_layer_workload"]}
+                                          for k in ("tiny_100_steps_ms", "single_layer_write_attend_ms")}}
     print(json.dumps(line))
 
 

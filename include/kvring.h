@@ -199,6 +199,17 @@ int kvring_snapshot(const kvring_t* ring, int32_t layer, uint8_t* host_k, uint8_
                     float* host_kamax, float* host_vamax, int32_t* host_pos,
                     int32_t* host_chunk, void* cuda_stream);
 
+/* Synchronous copy of the latest attention call's prepared queries (tests, debug):
+ * the e4m3 codes of Q rotated at its positions, quantised per (token, head) row
+ * with that row's own amax ([ai.info] "Latenza dei turni...": FP8 attention; the
+ * query side is quantised the same way as the cache).
+ *   host_q8:    uint8 [H][n_q][d] codes (may be NULL)
+ *   host_qamax: fp32  [H][n_q] row amax, the largest |q| of the rotated row (may be NULL)
+ * n_q is the latest kvring_attend's n_q.  Enqueues the copies on cuda_stream and
+ * synchronises it.  Errors: EINVAL (NULL ring, host-only ring), ESTATE (no
+ * attention call yet), ECUDA. */
+int kvring_snapshot_q(const kvring_t* ring, uint8_t* host_q8, float* host_qamax, void* cuda_stream);
+
 /* Synchronise cuda_stream and read the ring's device error word, which kernels set
  * when a bounded wait runs out.  Returns KVRING_OK or KVRING_ETIMEOUT (and clears
  * the word; the message says which kernel and wait).  Errors: EINVAL, ECUDA. */
@@ -231,17 +242,22 @@ int kvring_debug_fault(kvring_t* ring, int32_t skip_tile, int64_t timeout_ns);
  *   vt8:   e4m3 codes [H][d][slots_padded], slot-contiguous rows
  *   kamax, vamax: fp32 [H][slots_padded], the chunk amax of each slot
  *          (scale = amax / 448, amax 0 meaning scale 1)
- *   rope:  fp32 (cos, sin) pairs [rows][d/2] with rows > q_pos0 + n_q - 1;
- *          entry [p][i] = fp32(cos(p * w_i)), fp32(sin(p * w_i)), angle and
- *          cosine in float64, w_i = theta^(-2i/d) (the table kvring_create builds)
+ *   rope:  fp32 (cos, sin) pairs [rope_rows][d/2]; entry [p][i] = fp32(cos(p * w_i)),
+ *          fp32(sin(p * w_i)), angle and cosine in float64, w_i = theta^(-2i/d)
+ *          (the table kvring_create builds).  The queries read rows q_pos0 ..
+ *          q_pos0 + n_q - 1, so rope_rows >= q_pos0 + n_q (checked: EINVAL).
  *   q_bf16: [n_q][H][d]; query i sits at position q_pos0 + i
  *   out_f32: [n_q][H][d]
  * Slots [0, count) are attended; slots_padded is a multiple of 128 and the K
  * and V codes of slots [count, slots_padded) must be finite (zero will do): they
  * get weight exactly 0, but 0 times a NaN code is not 0.  k8, vt8, kamax,
  * vamax, q and out are 16-byte aligned.
- * err_word: 4 ints, set to KVRING_ETIMEOUT (and kernel, wait site, block) if a
- * bounded device wait runs out; NULL leaves such time-outs unreported.
+ * err_word: 4 ints, zero before the call.  If a bounded device wait runs out the
+ * kernel sets it to KVRING_ETIMEOUT (then kernel, wait site, block), but only
+ * while word 0 is still zero: the call does not clear it, so it keeps the first
+ * time-out of a series of calls until the caller zeroes it again.  NULL: the
+ * library's own word is used, cleared on the stream at the start of every call,
+ * and time-outs go unreported.
  *
  * Its only scratch is a fixed array inside the library (the e4m3 Q rows and
  * their amax): 16,384 rows of (head, query padded to 256), i.e. 2.06 MB that
@@ -255,7 +271,7 @@ int kvring_debug_fault(kvring_t* ring, int32_t skip_tile, int64_t timeout_ns);
  * kvring_attend.  Asynchronous on cuda_stream.  Errors (message in
  * kvring_last_error(NULL)): EINVAL, ENODEV, ECUDA. */
 int kvring_attend_noalloc(const void* k8, const void* vt8, const float* kamax, const float* vamax,
-                          const float* rope, int64_t q_pos0, const void* q_bf16, int32_t n_q,
+                          const float* rope, int64_t rope_rows, int64_t q_pos0, const void* q_bf16, int32_t n_q,
                           int32_t num_heads, int32_t head_dim, int32_t slots_padded, int32_t count,
                           float* out_f32, int* err_word, void* cuda_stream);
 

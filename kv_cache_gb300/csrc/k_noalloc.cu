@@ -72,7 +72,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 using namespace kvring_impl;
 
 extern "C" int kvring_attend_noalloc(const void* k8, const void* vt8, const float* kamax, const float* vamax,
-                                     const float* rope, int64_t q_pos0, const void* q_bf16, int32_t n_q,
+                                     const float* rope, int64_t rope_rows, int64_t q_pos0, const void* q_bf16, int32_t n_q,
                                      int32_t num_heads, int32_t head_dim, int32_t slots_padded, int32_t count,
                                      float* out_f32, int* err_word, void* cuda_stream) {
     if (n_q == 0) return KVRING_OK;
@@ -84,6 +84,10 @@ extern "C" int kvring_attend_noalloc(const void* k8, const void* vt8, const floa
         return noalloc_fail(KVRING_EINVAL, "slots_padded must be a positive multiple of 128");
     if (count < 1 || count > slots_padded) return noalloc_fail(KVRING_EINVAL, "count out of range [1, slots_padded]");
     if (n_q < 0 || q_pos0 < 0) return noalloc_fail(KVRING_EINVAL, "n_q and q_pos0 must be >= 0");
+    // Q prep reads rope rows q_pos0 .. q_pos0 + n_q - 1
+    if (rope_rows < 1 || q_pos0 > rope_rows - (int64_t)n_q)
+        return noalloc_fail(KVRING_EINVAL, "rope has " + std::to_string(rope_rows) + " rows; the queries need rows up to " +
+                                               std::to_string(q_pos0 + n_q - 1));
     const int64_t tstride = ((int64_t)n_q + 255) / 256 * 256;
     if ((int64_t)num_heads * tstride > kNoAllocMaxRows)
         return noalloc_fail(KVRING_EINVAL, "num_heads x n_q (padded to 256) = " + std::to_string(num_heads * tstride) +
@@ -110,6 +114,13 @@ extern "C" int kvring_attend_noalloc(const void* k8, const void* vt8, const floa
     uint8_t* q8 = scratch;
     float* qamax = reinterpret_cast<float*>(scratch + kNoAllocAmaxOff);
     int* err = err_word ? err_word : reinterpret_cast<int*>(scratch + kNoAllocErrOff);
+    // The library's own word (err_word NULL) starts every call at zero, so a
+    // time-out of an earlier call never masks one of this call; a caller's word
+    // is left as it is (it keeps the first time-out until the caller clears it).
+    if (!err_word) {
+        e = cudaMemsetAsync(err, 0, 4 * sizeof(int), s);
+        if (e != cudaSuccess) return noalloc_fail(KVRING_ECUDA, std::string("clearing the error word: ") + cudaGetErrorString(e));
+    }
 
     // Q prep writes every row of the Q scratch it uses (pad rows as zeros), so
     // nothing left by an earlier call is read.

@@ -68,6 +68,7 @@ struct kvring {
     // testing aid
     uint64_t launches = 0;
     int debug_skip_tile = -1;
+    int last_q_rows = 0;        // query rows of the latest attention call (for kvring_snapshot_q)
     long long debug_timeout_ns = 0;
     std::string error;
 };
@@ -554,6 +555,7 @@ int kvring_attend(kvring_t* r, int32_t layer, const void* q, int32_t n_q, float*
     e = launch_attend(ap, r->maps, s);
     if (e != cudaSuccess) return cuda_fail(r, e, "attention kernel launch");
     r->launches += 1;
+    r->last_q_rows = n_q;
     return KVRING_OK;
 }
 
@@ -676,6 +678,24 @@ int kvring_snapshot(const kvring_t* rc, int32_t layer, uint8_t* hk, uint8_t* hv,
         for (size_t h = 0; h < H; ++h)
             for (size_t dd = 0; dd < d; ++dd)
                 for (size_t sl = 0; sl < R; ++sl) hv[(h * R + sl) * d + dd] = vt[(h * d + dd) * R + sl];
+    return KVRING_OK;
+}
+
+int kvring_snapshot_q(const kvring_t* rc, uint8_t* hq, float* hqamax, void* stream) {
+    kvring_t* r = const_cast<kvring_t*>(rc);
+    if (!r) return KVRING_EINVAL;
+    if (r->host_only) return fail(r, KVRING_EINVAL, "no device data on a host-only ring");
+    if (r->last_q_rows <= 0) return fail(r, KVRING_ESTATE, "no attention call yet");
+    if (!hq && !hqamax) return KVRING_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t H = r->cfg.num_heads, d = r->cfg.head_dim, n = (size_t)r->last_q_rows, ts = (size_t)r->Tstride;
+    cudaError_t e = cudaSuccess;
+    if (hq) e = cudaMemcpy2DAsync(hq, n * d, r->q8, ts * d, n * d, H, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess && hqamax)
+        e = cudaMemcpy2DAsync(hqamax, n * sizeof(float), r->qamax, ts * sizeof(float), n * sizeof(float), H,
+                              cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(r, e, "Q snapshot copy");
     return KVRING_OK;
 }
 

@@ -87,12 +87,14 @@ _SIGNATURES = {
     "kvring_naive_refresh": (ctypes.c_int, [_P, ctypes.c_int32, _P]),
     "kvring_get_state": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.POINTER(kvring_state)]),
     "kvring_snapshot": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P]),
+    "kvring_snapshot_q": (ctypes.c_int, [_P, _P, _P, _P]),
     "kvring_check_device": (ctypes.c_int, [_P, _P]),
     "kvring_last_error": (ctypes.c_char_p, [_P]),
     "kvring_debug_fault": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int64]),
     "kvring_launch_count": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint64)]),
-    "kvring_attend_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int64, _P, ctypes.c_int32, ctypes.c_int32,
-                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P, _P]),
+    "kvring_attend_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int64, ctypes.c_int64, _P, ctypes.c_int32,
+                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P,
+                                             _P]),
 }
 
 
@@ -204,6 +206,14 @@ def kvring_snapshot(ring, layer: int, H: int, R: int, d: int, stream=None, cache
     return {"k": k, "v": v, "kamax": ka, "vamax": va, "pos": pos, "chunk": chunk}
 
 
+def kvring_snapshot_q(ring, n_q: int, H: int, d: int, stream=None) -> dict:
+    """Synchronous copy of the latest attention call's e4m3 Q codes [H, n_q, d] and row amax [H, n_q]."""
+    q8 = np.zeros((H, n_q, d), np.uint8)
+    qamax = np.zeros((H, n_q), np.float32)
+    _check(load().kvring_snapshot_q(ring, q8.ctypes.data, qamax.ctypes.data, _stream(stream)), ring)
+    return {"q8": q8, "qamax": qamax}
+
+
 def kvring_check_device(ring, stream=None) -> int:
     """KVRING_OK or KVRING_ETIMEOUT (returned, not raised); other codes raise."""
     rc = load().kvring_check_device(ring, _stream(stream))
@@ -227,28 +237,78 @@ def kvring_debug_fault(ring, skip_tile: int, timeout_ns: int) -> None:
     _check(load().kvring_debug_fault(ring, skip_tile, timeout_ns), ring)
 
 
+def noalloc_arg_error(k8, vt8, kamax, vamax, rope, q_pos0: int, q, out, count: int, err=None, device=None):
+    """The first problem with kvring_attend_noalloc's arguments, or None.
+
+    Checks every tensor's dtype, shape, contiguity and device (``device``: the
+    device the call will run on, by default the current CUDA device), that the
+    RoPE table has the rows the queries read, and that ``err`` is None or int32
+    with at least 4 elements.  The library repeats the checks it can make on raw
+    pointers (row counts, sizes, alignment); dtypes and devices only this layer sees.
+    """
+    import torch
+    if device is None:
+        if not torch.cuda.is_available():
+            return "no CUDA device is available"
+        device = torch.device("cuda", torch.cuda.current_device())
+    device = torch.device(device)
+    if not isinstance(q, torch.Tensor) or q.dim() != 3:
+        return "q must be a tensor of shape (n_q, H, d)"
+    n_q, H, d = (int(x) for x in q.shape)
+    if not isinstance(k8, torch.Tensor) or k8.dim() != 3:
+        return "k8 must be a tensor of shape (H, slots_padded, d)"
+    slots_padded = int(k8.shape[1])
+    spec = (("q", q, torch.bfloat16, (n_q, H, d)), ("k8", k8, torch.uint8, (H, slots_padded, d)),
+            ("vt8", vt8, torch.uint8, (H, d, slots_padded)), ("kamax", kamax, torch.float32, (H, slots_padded)),
+            ("vamax", vamax, torch.float32, (H, slots_padded)), ("out", out, torch.float32, (n_q, H, d)))
+    for name, t, dtype, shape in spec:
+        if not isinstance(t, torch.Tensor):
+            return f"{name} must be a torch tensor"
+        if t.dtype != dtype:
+            return f"{name} must be {dtype}, got {t.dtype}"
+        if tuple(t.shape) != shape:
+            return f"{name} must have shape {shape}, got {tuple(t.shape)}"
+        if not t.is_contiguous():
+            return f"{name} must be contiguous"
+        if t.device != device:
+            return f"{name} is on {t.device}, the call runs on {device}"
+    if not isinstance(rope, torch.Tensor) or rope.dtype != torch.float32 or rope.dim() != 3 \
+            or tuple(rope.shape[1:]) != (d // 2, 2) or not rope.is_contiguous():
+        return f"rope must be a contiguous float32 tensor of shape (rows, {d // 2}, 2)"
+    if rope.device != device:
+        return f"rope is on {rope.device}, the call runs on {device}"
+    if int(q_pos0) < 0 or int(rope.shape[0]) < int(q_pos0) + n_q:
+        return f"rope has {int(rope.shape[0])} rows; queries at positions {int(q_pos0)}..{int(q_pos0) + n_q - 1} need more"
+    if not 1 <= int(count) <= slots_padded:
+        return f"count must be in [1, {slots_padded}]"
+    if err is not None:
+        if not isinstance(err, torch.Tensor) or err.dtype != torch.int32 or err.numel() < 4 or not err.is_contiguous():
+            return "err must be None or a contiguous int32 tensor of at least 4 elements"
+        if err.device != device:
+            return f"err is on {err.device}, the call runs on {device}"
+    return None
+
+
 def kvring_attend_noalloc(k8, vt8, kamax, vamax, rope, q_pos0: int, q, out, count: int, err=None,
                           stream=None) -> None:
     """Attention over a caller-held one-layer cache without any device allocation.
 
     k8 uint8 [H, slots_padded, d], vt8 uint8 [H, d, slots_padded], kamax/vamax
-    float32 [H, slots_padded], rope float32 [rows, d/2, 2], q bf16 [n_q, H, d],
-    out float32 [n_q, H, d], err int32 [4] or None -- all CUDA tensors the caller
-    owns (see include/kvring.h for the layouts and the fixed scratch limit).
+    float32 [H, slots_padded], rope float32 [rows, d/2, 2] with rows >= q_pos0 + n_q,
+    q bf16 [n_q, H, d], out float32 [n_q, H, d], err int32 [>= 4] (zero before the
+    call; it keeps the first time-out) or None -- all CUDA tensors the caller owns,
+    on the current device (include/kvring.h has the layouts and the fixed scratch
+    limit).  Bad arguments raise ValueError before anything is launched.
     """
+    msg = noalloc_arg_error(k8, vt8, kamax, vamax, rope, q_pos0, q, out, count, err)
+    if msg is not None:
+        raise ValueError(msg)
     n_q, H, d = (int(x) for x in q.shape)
     slots_padded = int(k8.shape[1])
-    qp = _dev_bf16(q, n_q, H, d, "q")
-    for name, t, shape in (("k8", k8, (H, slots_padded, d)), ("vt8", vt8, (H, d, slots_padded)),
-                           ("kamax", kamax, (H, slots_padded)), ("vamax", vamax, (H, slots_padded)),
-                           ("out", out, (n_q, H, d))):
-        if not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != shape:
-            raise ValueError(f"{name} must be a contiguous CUDA tensor of shape {shape}")
-    if not rope.is_cuda or not rope.is_contiguous() or rope.shape[1:] != (d // 2, 2):
-        raise ValueError(f"rope must be a contiguous CUDA tensor of shape (rows, {d // 2}, 2)")
     rc = load().kvring_attend_noalloc(k8.data_ptr(), vt8.data_ptr(), kamax.data_ptr(), vamax.data_ptr(),
-                                      rope.data_ptr(), int(q_pos0), qp, n_q, H, d, slots_padded, int(count),
-                                      out.data_ptr(), err.data_ptr() if err is not None else None, _stream(stream))
+                                      rope.data_ptr(), int(rope.shape[0]), int(q_pos0), q.data_ptr(), n_q, H, d,
+                                      slots_padded, int(count), out.data_ptr(),
+                                      err.data_ptr() if err is not None else None, _stream(stream))
     _check(rc, None)
 
 
@@ -267,6 +327,7 @@ class KVRing:
                                  max_position, rope_theta, flags, S, W, pt, ph)
         self.L, self.H, self.d, self.R = num_layers, num_heads, head_dim, capacity
         self.host_only = host_only
+        self._last_nq = 0
         self.handle = kvring_create(self.cfg)
 
     def close(self) -> None:
@@ -300,6 +361,7 @@ class KVRing:
         if out is None:
             out = torch.empty((q.shape[0], self.H, self.d), dtype=torch.float32, device=q.device)
         kvring_attend(self.handle, layer, q, q.shape[0], out, self.H, self.d, stream)
+        self._last_nq = int(q.shape[0])
         return out
 
     def rebase(self, stream=None) -> None:
@@ -314,6 +376,10 @@ class KVRing:
 
     def snapshot(self, layer: int, stream=None, cache: bool = True) -> dict:
         return kvring_snapshot(self.handle, layer, self.H, self.R, self.d, stream, cache)
+
+    def snapshot_q(self, stream=None) -> dict:
+        """The latest attention call's prepared queries (e4m3 codes and row amax)."""
+        return kvring_snapshot_q(self.handle, self._last_nq, self.H, self.d, stream)
 
     def check_device(self, stream=None) -> int:
         return kvring_check_device(self.handle, stream)

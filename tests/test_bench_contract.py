@@ -25,6 +25,11 @@ def test_reference_arm_prints_one_contract_line():
     up = j["cpu_baseline"]["upkeep"]          # the CPU analogue of the pages' upkeep comparison
     assert up["naive_ms_per_step"] > up["write_time_ms_per_step"] > 0
     assert j["e2e"] == {"value": j["value"], "unit": j["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    # one block step timed: 1/60 of a full step, extrapolated x60, and said so
+    assert j["block_steps_timed"] == 1 and abs(j["steps"] - 1 / 60) < 1e-12
+    assert j["extrapolated"] is True and j["extrapolation_factor"] == 60
+    assert abs(j["ms_per_step"] - 60 * j["cpu_baseline"]["block_step_ms"][0]) < 1e-6
+    assert j["cpu_baseline"]["whole"]["tiny_100_steps_ms"] > 0
     assert j["config"]["workload"].startswith("steady denoise step")
 
 
@@ -71,10 +76,15 @@ def test_gpu_arm_line_has_every_contract_key(monkeypatch, capsys):
     K = 42
     fake = dict(ms=15.4 * K, w_ms=[0.0166] * 60, a_ms=[0.0631] * 240, r_ms=[], rb_ms=0.275, launches=25201,
                 clocks={"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 4},
-                e2e_ms=16.1 * 12, e2e_steps=12, h2d=1116241920, d2h=24805376)
+                e2e_ms=16.1 * 12, e2e_steps=12, h2d=1116241920, d2h=1488322560, resets_timed=1)
     monkeypatch.setattr(bench, "run_gpu", lambda args, cfg, rank, world: fake)
     monkeypatch.setattr(bench, "oracle_sample", lambda cfg: {"block_s": 6.6, "step_s": 397.0, "cores": 16,
                                                              "cpu_model": "host", "sample": "one block"})
+    monkeypatch.setattr(bench, "oracle_whole_configs", lambda: {
+        "tiny_100_steps_ms": 900.0, "single_layer_write_attend_ms": 1500.0, "tiny_workload": "tiny",
+        "single_layer_workload": "one layer"})
+    monkeypatch.setattr(bench, "run_whole_configs_gpu", lambda: {"tiny_100_steps_ms": 4.0,
+                                                                 "single_layer_write_attend_ms": 0.08})
     monkeypatch.setattr(bench, "oracle_upkeep_sample", lambda cfg: {"naive_ms_per_step": 6.8e5,
                                                                     "write_time_ms_per_step": 2.0e4, "ratio": 34.0,
                                                                     "sample": "one block"})
@@ -100,6 +110,10 @@ def test_gpu_arm_line_has_every_contract_key(monkeypatch, capsys):
     assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-12
     cb = j["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] == 16 and cb["upkeep"]["ratio"] == 34.0
+    # configurations 1 and 2 timed whole on both sides
+    assert cb["whole"]["tiny_100_steps_ms"] == {"cpu_ms": 900.0, "gpu_ms": 4.0, "workload": "tiny"}
+    assert cb["whole"]["single_layer_write_attend_ms"]["gpu_ms"] == 0.08
+    assert j["resets_in_timed_steps"] == 1
     assert j["clocks"]["sm_mhz"] == 2070.0
 
 
@@ -117,3 +131,29 @@ def test_rebase_stress_line_counts_only_the_bytes_a_reset_moves(monkeypatch, cap
         assert j["value"] == 0.25 and j["higher_is_better"] is False
         assert abs(j["roofline"]["achieved"] - nbytes / 0.25e-3 / 1e9) < 1e-6
         assert ("3-D" in j["config"]["workload"]) == bool(extra)
+
+
+def test_session_line_reports_step_times_and_drift(monkeypatch, capsys):
+    """--session (the unsharded-width session): per-step median and p99, the
+    breakdown, and the drift checkpoints with the rule that judges them."""
+    sys.path.insert(0, ROOT)
+    import bench
+    drift = [{"step": s, "block": b, "bookkeeping_exact": True, "k_identical": 1.0, "v_identical": 1.0,
+              "k_max_steps": 0.0, "attn_max_abs": 4e-3 if s == 1 else 5e-3, "attn_mean_rel": 1e-4}
+             for s in (1, 41, 42, 43, 500, 999) for b in (0, 59)]
+    fake = dict(step_ms=[20.0] * 980 + [25.0] * 20, drift=drift, clocks={"sm_mhz": 2070.0, "reasons": []},
+                w_ms=[0.04] * 60, a_ms=[0.08] * 240, rb_ms=1.0)
+    monkeypatch.setattr(bench, "run_session", lambda args, cfg: fake)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--session"])
+    bench.main()
+    j = json.loads([l for l in capsys.readouterr().out.splitlines() if l.startswith("{")][0])
+    assert j["unit"] == "ms/step" and j["higher_is_better"] is False and j["steps"] == 1000
+    assert j["step_ms"]["median"] == 20.0 and j["step_ms"]["p99"] == 25.0
+    assert abs(j["value"] - (980 * 20 + 20 * 25) / 1000) < 1e-9
+    assert j["config"]["heads"] == 64 and j["config"]["attention_calls_per_step"] == 240
+    assert j["no_drift"] is True and len(j["drift"]) == 12
+    assert abs(j["breakdown"]["rebase_gbs"] - 2 * 60 * 64 * 5788 * 128 / 1e-3 / 1e9) < 1e-6
+    fake["drift"][-1]["k_identical"] = 0.99
+    bench.main()
+    j = json.loads([l for l in capsys.readouterr().out.splitlines() if l.startswith("{")][0])
+    assert j["no_drift"] is False

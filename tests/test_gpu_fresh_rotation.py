@@ -1,0 +1,115 @@
+"""The GPU rebase against a fresh rotation, and the GPU Q preparation against the oracle's.
+
+A position reset turns every cached K by -delta in place, from its FP8 codes
+(ai.info, "Characters funziona in tempo reale su quattro H100", section "La
+gestione della cache spostata al momento della scrittura": one delta rotation
+of the cached window per reset).  The bar for it is distance to a fresh
+rotation: the naive window's codes, which re-rotate the original bf16 K at the
+new positions.  Here at the production shape (16 heads x 128, 5,788 slots,
+757-token chunks, 1 % x20 outliers) and the production deltas: 26,006 at the
+first reset (before step 42's write) and 31,794 at every later one.
+
+* every rebased code is within one e4m3 step of the fresh rotation, the step
+  taken at the pair's norm (the magnitude a rotation keeps); the codes are
+  bit-exact with the oracle's own delta rotation;
+* the identical fraction, and the worst distance by the element's own step and
+  by the step of the fresh pair's larger element, are printed.
+
+Q preparation (RoPE at the latest chunk's positions, one e4m3 scale per
+(token, head) row) is compared code for code with the oracle's.
+"""
+import numpy as np
+import pytest
+
+from kv_cache_gb300 import kvring as kv
+from oracle import e4m3
+from oracle.schemes import NaiveWindow, WriteTimeRing, quantise_q
+from tests._lib import ensure_built
+from tests.gpu_util import chunk_pair, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_built()
+
+
+def _logical(snap_k, head, count, R):
+    idx = (head - count + np.arange(count)) % R
+    return snap_k[:, idx]
+
+
+def _steps(a_codes, b_codes):
+    """Distances |a - b| in e4m3 steps: at b's pair norm, at b's pair's larger element, at the element itself."""
+    a, b = e4m3.decode(a_codes), e4m3.decode(b_codes)
+    diff = np.abs(a - b)
+    b0, b1 = b[..., 0::2], b[..., 1::2]
+    norm = np.repeat(np.sqrt(b0 ** 2 + b1 ** 2), 2, axis=-1)
+    larger = np.repeat(np.maximum(np.abs(b0), np.abs(b1)), 2, axis=-1)
+    own = np.maximum(np.abs(a), np.abs(b))
+    return diff / e4m3.ulp_at(norm), diff / e4m3.ulp_at(larger), diff / e4m3.ulp_at(own)
+
+
+def test_rebase_production_deltas_against_fresh_rotation():
+    R, T, H, d = 5788, 757, 16, 128
+    ring = kv.KVRing(1, H, d, R, T, max_position=R + 42 * T)
+    naive = NaiveWindow(R, H, d)
+    exact = WriteTimeRing(R, H, d)
+    deltas = []
+    for s in range(85):
+        if s > 0 and s % 42 == 0:
+            st = ring.state(0)
+            ring.rebase()
+            deltas.append(naive.rebase())
+            assert exact.rebase() == deltas[-1] == st["next_pos"] - st["count"]
+            snap = ring.snapshot(0)
+            st = ring.state(0)
+            assert st["next_pos"] == st["count"] == R
+            assert np.array_equal(snap["k"], exact.k8), f"reset at step {s}: not the oracle's delta rotation"
+            assert np.array_equal(snap["v"], exact.v8)
+            k8, v8, _, _ = naive.cache_codes()
+            got = _logical(snap["k"], st["head"], st["count"], R)
+            fresh = k8.transpose(1, 0, 2)
+            by_norm, by_larger, by_own = _steps(got, fresh)
+            same = float(np.mean(got == fresh))
+            print(f"reset at step {s}, delta {deltas[-1]}: identical {same:.5f}; worst {by_norm.max():.0f} step "
+                  f"at the pair norm, {by_larger.max():.0f} at the pair's larger element "
+                  f"({int(np.sum(by_larger > 1))} of {by_larger.size} past 1), {by_own.max():.0f} at the element's own")
+            assert by_norm.max() <= 1.0, f"reset at step {s}: {by_norm.max()} steps from a fresh rotation"
+            assert by_larger.max() <= 2.0 and np.mean(by_larger <= 1.0) >= 0.99999
+            assert np.array_equal(_logical(snap["v"], st["head"], st["count"], R), v8.transpose(1, 0, 2))
+            # the positions of the window are [0, count) again
+            assert np.array_equal(np.sort(snap["pos"]), np.arange(R))
+        kb, kf = chunk_pair("k", 4000 + s, T, H, d, True)
+        vb, vf = chunk_pair("v", 4000 + s, T, H, d, True)
+        ring.write(0, to_dev(kb), to_dev(vb))
+        naive.write(kf, vf)
+        exact.write(kf, vf)
+    assert deltas == [26006, 31794]
+    assert ring.check_device() == kv.KVRING_OK
+    ring.close()
+
+
+@pytest.mark.parametrize("R,T,H,d,writes", [(5788, 757, 16, 128, 44), (96, 32, 2, 64, 3), (300, 130, 3, 128, 5)])
+def test_qprep_codes_match_oracle(R, T, H, d, writes):
+    """Q rotated at the latest chunk's positions and quantised per (token, head) row:
+    codes and row amax bit-exact with the oracle, before and after a reset."""
+    ring = kv.KVRing(1, H, d, R, T, max_position=R + 44 * T)
+    for w in range(writes):
+        if w == writes - 1:
+            ring.rebase()
+        kb, _ = chunk_pair("k", 4100 + w, T, H, d, True)
+        vb, _ = chunk_pair("v", 4100 + w, T, H, d, True)
+        ring.write(0, to_dev(kb), to_dev(vb))
+        if w in (writes - 2, writes - 1):
+            qb, qf = chunk_pair("q", 4100 + w, T, H, d, True)
+            ring.attend(0, to_dev(qb))
+            st = ring.state(0)
+            got = ring.snapshot_q()
+            codes, amax = quantise_q(qf, st["last_write_pos"] + np.arange(T), d, 10000.0)
+            assert np.array_equal(got["qamax"], amax.T), f"write {w}: Q row amax"
+            assert np.array_equal(got["q8"], codes.transpose(1, 0, 2)), (
+                f"write {w}: Q codes, {np.mean(got['q8'] == codes.transpose(1, 0, 2)):.6f} identical")
+    assert ring.check_device() == kv.KVRING_OK
+    ring.close()

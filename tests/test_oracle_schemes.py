@@ -36,6 +36,18 @@ def _pair_ulp_diff(a_codes, b_codes):
     return np.abs(a - b) / e4m3.ulp_at(mag)
 
 
+def _pair_norm_ulp_diff(a_codes, b_codes):
+    """|decode(a) - decode(b)| in units of the e4m3 step at the norm of b's pair.
+
+    A RoPE pair is a 2-D vector; a rotation keeps its norm and moves its larger
+    element anywhere between norm / sqrt(2) and norm, so the norm is the one
+    magnitude the cached pair and a fresh rotation of it share."""
+    a = e4m3.decode(a_codes)
+    b = e4m3.decode(b_codes)
+    norm = np.sqrt(b[..., 0::2] ** 2 + b[..., 1::2] ** 2)
+    return np.abs(a - b) / e4m3.ulp_at(np.repeat(norm, 2, axis=-1))
+
+
 def test_amax_k_is_largest_pair_norm_bruteforce():
     x = _chunk("k", 0, 5, 2, 8, outliers=True)
     got = chunk_amax_k(x)
@@ -139,6 +151,39 @@ def test_rebase_within_one_pair_step_of_fresh_rotation(R, T, H, d):
     # the worst case is hundreds of steps, since the rotation moves the large
     # partner's rounding error into the small one
     assert worst == 1.0
+
+
+def test_rebase_within_one_pair_step_at_production_deltas():
+    """d = 128, the production ring (5,788 slots, 757-token chunks) and its reset
+    deltas: the first reset (before step 42's write) moves the window by
+    42 x 757 - 5,788 = 26,006 positions, every later one by 42 x 757 = 31,794.
+    Two heads keep the run short; the deltas and the rotation angles are the
+    production ones.  Every delta-rotated code is within one e4m3 step of a
+    fresh rotation at the new positions, the step taken at the pair's norm.
+    Taken at the fresh pair's larger element instead, a handful of the 1.48 M
+    codes per reset are two steps apart: there the rotation has moved the larger
+    element one binade below the norm, while the cached codes still carry the
+    rounding of the pair before the rotation."""
+    R, T, H, d = 5788, 757, 2, 128
+    naive = NaiveWindow(R, H, d)
+    ring = WriteTimeRing(R, H, d)
+    deltas = []
+    for s in range(85):
+        if s > 0 and s % 42 == 0:
+            deltas.append(ring.rebase())
+            assert naive.rebase() == deltas[-1]
+            k8, _, _, _ = naive.cache_codes()
+            fresh = k8.transpose(1, 0, 2)
+            got = _logical(ring, ring.k8)
+            assert _pair_norm_ulp_diff(got, fresh).max() == 1.0, s
+            by_larger = _pair_ulp_diff(got, fresh)
+            assert by_larger.max() <= 2.0 and np.mean(by_larger <= 1.0) >= 0.99999, s
+            assert np.mean(got == fresh) > 0.6, s
+        k = _chunk("k", 3000 + s, T, H, d, outliers=True)
+        v = _chunk("v", 3000 + s, T, H, d, outliers=True)
+        naive.write(k, v)
+        ring.write(k, v)
+    assert deltas == [26006, 31794]
 
 
 def test_attention_nearly_unchanged_by_a_reset():
