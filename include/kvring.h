@@ -124,7 +124,11 @@ int kvring_destroy(kvring_t* ring);
 
 /* Write one chunk of n_tokens new tokens into layer `layer`'s ring
  * ([ai.info] "La gestione della cache..."; [neurocartel] "Кэш...").
- *   k_bf16, v_bf16: device, bf16 [n_tokens][H][d], token-major, contiguous.
+ *   k_bf16, v_bf16: device, bf16 [n_tokens][H][d], token-major, contiguous,
+ *                   16-byte aligned (EINVAL otherwise).
+ * One kernel launch: one cluster of 8 CTAs per (head, K|V), each CTA reading its
+ * share of the chunk once into shared memory; the chunk amax is exchanged
+ * between the CTAs of a cluster through distributed shared memory.
  * Token j goes to slot (head + j) mod R at position next_pos + j; the oldest slots
  * are overwritten, nothing is copied.  K is rotated by RoPE at its position and
  * both K and V are quantised to FP8 e4m3 with one scale per (head, chunk):
@@ -132,7 +136,7 @@ int kvring_destroy(kvring_t* ring);
  * code = e4m3_rne_satfinite(x * (448/amax)).  The chunk's amax is stored with
  * each of its slots and never changes.
  * Then head += n (mod R), count = min(count + n, R), next_pos += n.
- * n_tokens == 0 is a no-op.  Errors: EINVAL (layer, pointers, n_tokens >
+ * n_tokens == 0 is a no-op.  Errors: EINVAL (layer, pointers or their alignment, n_tokens >
  * max_tokens_per_write, or not a whole number of frames on a 3-D ring), ESTATE
  * (next_pos + n_tokens > max_position), ECUDA. */
 int kvring_write(kvring_t* ring, int32_t layer, const void* k_bf16, const void* v_bf16,

@@ -65,6 +65,7 @@ struct kvring {
     float* vaw = nullptr;
     int* err = nullptr;         // [4]
     AttendMaps maps{};
+    CUtensorMap rope_map{};     // the RoPE table for the write kernel
     // testing aid
     uint64_t launches = 0;
     int debug_skip_tile = -1;
@@ -145,20 +146,8 @@ void build_rope_table(std::vector<float2>& tab, int max_pos, int d, double theta
 
 int make_map(kvring_t* r, CUtensorMap* map, void* base, const cuuint64_t dims[3], const cuuint64_t strides[2],
              const cuuint32_t box[3], CUtensorMapSwizzle swz) {
-    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-    if (!encode) {
-        void* fn = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
-            return fail(r, KVRING_ECUDA, "cuTensorMapEncodeTiled entry point not available");
-        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-    const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult res = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (res != CUDA_SUCCESS) return fail(r, KVRING_ECUDA, "cuTensorMapEncodeTiled failed: " + std::to_string((int)res));
+    const int rc = kvring_impl::encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, swz);
+    if (rc) return fail(r, rc, "cuTensorMapEncodeTiled failed");
     return KVRING_OK;
 }
 
@@ -276,6 +265,22 @@ int naive_write(kvring_t* r, int layer, const void* k, const void* v, int n, boo
 }  // namespace
 
 namespace kvring_impl {
+int encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank, void* base, const cuuint64_t* dims,
+                 const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return KVRING_ECUDA;
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult res = encode(map, dtype, (cuuint32_t)rank, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS ? KVRING_OK : KVRING_ECUDA;
+}
+
 // Message reported by kvring_last_error(NULL) for calls that have no ring.
 void set_thread_error(const std::string& msg) { g_create_error = msg; }
 
@@ -390,7 +395,10 @@ int kvring_create(const kvring_config* cfg_in, kvring_t** out) {
         const cuuint32_t qbox[3] = {(cuuint32_t)d, 128, 1};
         if ((rc = make_map(nullptr, &r->maps.k8, r->k8, kdims, kstr, kbox, swz_d)) ||
             (rc = make_map(nullptr, &r->maps.vt8, r->vt8, vdims, vstr, vbox, CU_TENSOR_MAP_SWIZZLE_128B)) ||
-            (rc = make_map(nullptr, &r->maps.q8, r->q8, qdims, qstr, qbox, swz_d))) {
+            (rc = make_map(nullptr, &r->maps.q8, r->q8, qdims, qstr, qbox, swz_d)) ||
+            (cudaSuccess != write_setup() && (rc = fail(nullptr, KVRING_ECUDA, "write kernel attributes"))) ||
+            ((rc = write_rope_map(&r->rope_map, r->rope, cfg.max_position, (int)d)) &&
+             (rc = fail(nullptr, rc, "tensor map of the RoPE table")))) {
             free_device(r);
             delete r;
             return rc;
@@ -422,6 +430,8 @@ int kvring_write_ex(kvring_t* r, int32_t layer, const void* k, const void* v, in
     if (rewrite && n != L.last_n) return fail(r, KVRING_ESTATE, "a rewrite must have the latest write's n_tokens");
     if (n == 0) return KVRING_OK;
     if (!r->host_only && (!k || !v)) return fail(r, KVRING_EINVAL, "k or v is NULL");
+    if (!r->host_only && ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15))
+        return fail(r, KVRING_EINVAL, "k and v must be 16-byte aligned");
     if (!rewrite && L.next_pos + n > c.max_position)
         return fail(r, KVRING_ESTATE, "positions would reach max_position: call kvring_rebase first");
     if (r->naive) return naive_write(r, layer, k, v, n, rewrite, stream);
@@ -462,9 +472,13 @@ int kvring_write_ex(kvring_t* r, int32_t layer, const void* k, const void* v, in
         p.amax_tokens_per_block = write_amax_tokens_per_block(p.H, p.d);
         p.amax_blocks = (n + p.amax_tokens_per_block - 1) / p.amax_tokens_per_block;
         p.part = r->wpart;
+        p.err = r->err;
+        p.timeout_ns = 2000000000LL;
+        p.ropemap = r->rope_map;
+        if (write_input_maps(p) != KVRING_OK) return fail(r, KVRING_ECUDA, "tensor maps of the chunk's K and V");
         cudaError_t e = launch_write(p, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(r, e, "write kernel launch");
-        r->launches += 2;
+        r->launches += 1;
     }
     if (rewrite) return KVRING_OK;   // same slots, positions and chunk id: nothing moves
     for (int j = 0; j < n; ++j) {
@@ -710,9 +724,16 @@ int kvring_check_device(kvring_t* r, void* stream) {
     if (w[0] == 0) return KVRING_OK;
     static const char* sites[] = {"?", "Q tiles", "K/V stage full", "K/V stage free", "S", "P", "O", "fp16 V full",
                                   "fp16 V free", "the other KV splits"};
-    const int site = (w[2] >= 0 && w[2] <= 9) ? w[2] : 0;
-    r->error = std::string("device wait timed out in the attention kernel (wait for ") + sites[site] +
-               ", block " + std::to_string(w[3]) + ")";
+    static const char* write_sites[] = {"?", "the chunk's rows", "the chunk amax from the cluster"};
+    if (w[1] == kKernelWrite) {
+        const int site = (w[2] >= 0 && w[2] <= 2) ? w[2] : 0;
+        r->error = std::string("device wait timed out in the write kernel (wait for ") + write_sites[site] +
+                   ", block " + std::to_string(w[3]) + ")";
+    } else {
+        const int site = (w[2] >= 0 && w[2] <= 9) ? w[2] : 0;
+        r->error = std::string("device wait timed out in the attention kernel (wait for ") + sites[site] +
+                   ", block " + std::to_string(w[3]) + ")";
+    }
     e = cudaMemset(r->err, 0, sizeof(w));
     // a CTA that gave up may have left a split counter behind
     if (e == cudaSuccess)

@@ -16,10 +16,13 @@ constexpr float kE4M3Max = 448.0f;
 
 // Device error word: [0] = status (0 or KVRING_ETIMEOUT), [1] = kernel id,
 // [2] = wait site, [3] = block index that gave up.
-enum KernelId : int { kKernelAttend = 1 };
+enum KernelId : int { kKernelAttend = 1, kKernelWrite = 2 };
 
 // ---------------------------------------------------------------- write (K1)
 struct WriteParams {
+    CUtensorMap kmap;         // the chunk's K, 3-D {d, H, T} bf16 (as u16), box {d, 1, 16}
+    CUtensorMap vmap;         // the chunk's V, the same
+    CUtensorMap ropemap;      // the RoPE table, 2-D {d (u32: d/2 cos-sin pairs), max_position}, box {d, 16}
     const uint16_t* k;        // bf16 [T][H][d]
     const uint16_t* v;        // bf16 [T][H][d]
     uint8_t* k8;              // this layer's K ring  [H][Rpad][d]
@@ -36,9 +39,15 @@ struct WriteParams {
     int amax_tokens_per_block;
     int amax_blocks;          // ceil(T / amax_tokens_per_block)
     float* part;              // per-block amax partials [K|V][amax_blocks][H] (ring scratch)
+    int* err;                 // the ring's device error word
+    long long timeout_ns;     // bound of each device wait
 };
-cudaError_t launch_write(const WriteParams& p, cudaStream_t s);   // two launches
-cudaError_t launch_write_amax(const WriteParams& p, cudaStream_t s);   // the first of them alone
+cudaError_t write_setup();                                        // function attributes, once per device
+cudaError_t launch_write(const WriteParams& p, cudaStream_t s);   // one launch (clusters)
+// Tensor maps of a write: the chunk's K and V (per call) and the RoPE table (per ring).
+int write_input_maps(WriteParams& p);
+int write_rope_map(CUtensorMap* map, const float2* rope, int64_t max_position, int d);
+cudaError_t launch_write_amax(const WriteParams& p, cudaStream_t s);   // chunk amax partials (naive scheme)
 int write_amax_tokens_per_block(int H, int d);
 
 // ---------------------------------------------------------------- naive upkeep (comparison)
@@ -138,6 +147,10 @@ size_t attend_smem_bytes(int d);
 
 // Shared by the host translation units.
 void set_thread_error(const std::string& msg);
+// Tiled tensor map (no swizzle unless given, 256-byte L2 promotion, zeros out of
+// bounds); KVRING_OK or KVRING_ECUDA.  strides: rank - 1 byte strides.
+int encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank, void* base, const cuuint64_t* dims,
+                 const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz);
 int encode_u8_map(CUtensorMap* map, void* base, const cuuint64_t dims[3], const cuuint64_t strides[2],
                   const cuuint32_t box[3], CUtensorMapSwizzle swz);
 

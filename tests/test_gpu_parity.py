@@ -62,6 +62,24 @@ def test_write_production_shape():
     assert fk == 1.0 and fv == 1.0
 
 
+@pytest.mark.parametrize("R,T,H,d,writes", [(300, 290, 3, 128, 5), (4100, 2048, 2, 128, 4), (2100, 2048, 1, 64, 3),
+                                             (61, 50, 2, 64, 6)])
+def test_write_long_chunks(R, T, H, d, writes):
+    """Chunks of more than R - 16 tokens (their end wraps into the 16-slot group of
+    their first slot) and of 2,048 tokens (17 groups per CTA of a cluster of 8):
+    codes and amax bit-exact with the oracle after every write."""
+    ring = kv.KVRing(1, H, d, R, T, max_position=T * (writes + 1))
+    o = WriteTimeRing(R, H, d)
+    for w in range(writes):
+        kb, kf = chunk_pair("k", 300 + w, T, H, d, True)
+        vb, vf = chunk_pair("v", 300 + w, T, H, d, True)
+        ring.write(0, to_dev(kb), to_dev(vb))
+        o.write(kf, vf)
+        fk, fv = _check_cache(ring, 0, o)
+        assert fk == 1.0 and fv == 1.0, f"write {w}: {fk}, {fv}"
+    assert ring.check_device() == kv.KVRING_OK
+
+
 # (600, 150, 2, 64): as the ring fills, 2, 3, 4 and 3 KV splits, merged as clusters
 @pytest.mark.parametrize("R,T,H,d", [(96, 32, 2, 64), (100, 32, 2, 64), (300, 100, 2, 128), (600, 150, 2, 64)])
 def test_attend_small(R, T, H, d):
