@@ -17,7 +17,7 @@ A "step" is one pass of the whole hot path: [rebase when due] + 60 x write +
 * The timed steps start at a reset step (positions reset before that step's
   writes), so K timed steps hold ceil(K / 42) rebases: at least the reset's
   share of the path, never less.
-* roofline: the attention call (one launch: Q prep, attention and split merge),
+* roofline: the attention call (Q-prep + attention + split combine launches),
   algorithmic FLOP 4*T*R*d*H per call at a full ring, against the measured
   bf16 peak x 2 (FP8); plus the write kernel against measured HBM bandwidth.
 * cpu_baseline / --impl reference: the CPU oracle (naive per-call upkeep, then
@@ -976,7 +976,7 @@ def main():
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": fp8_sustained, "unit": "TFLOP/s",
                      "frac": attn_tflops / fp8_sustained, "traffic": attend_traffic(cfg),
                      "traffic_unit": "bytes per attend_kernel launch (ncu, 8-block run)",
-                     "kernel": "attention call (one launch: Q prep, attention, split merge)",
+                     "kernel": "attention call (q-prep + attention + split combine)",
                      "peak_source": f"{peak_src}: 2 x bf16_tflops_sustained (FP8 = 2 x bf16 nominal ratio)"},
         "breakdown": {
             "upkeep_ms_per_step": w_avg * L * cfg["writes_per_step"] + (sum(r["r_ms"]) / K if r["r_ms"] else 0.0),

@@ -24,7 +24,7 @@
  *     stream reaches the call.  All calls on one ring must be ordered on a single
  *     stream by the caller (the ring's scratch buffers are shared between calls).
  *   - The ring owns every device buffer it allocates (FP8 K and V rings, per-slot
- *     chunk amax, RoPE table, split partials, error word).  The caller
+ *     chunk amax, RoPE table, Q scratch, split partials, error word).  The caller
  *     owns every buffer it passes in.
  *   - Layouts: token-major bf16 [n][H][d] for K, V, Q inputs; fp32 [n][H][d] for
  *     the attention output.  All element counts are in elements, not bytes.
@@ -165,11 +165,9 @@ int kvring_write_ex(kvring_t* ring, int32_t layer, const void* k_bf16, const voi
 /* Attention of the latest chunk's queries over the finished FP8 cache of `layer`
  * ([wechild] paragraph 6; [ai.info] "Latenza dei turni...": FP8 attention that
  * accepts per-head scales).
- *   q_bf16:  device, bf16 [n_q][H][d], 16-byte aligned; query i sits at position
- *            last_write_pos + i.
+ *   q_bf16:  device, bf16 [n_q][H][d]; query i sits at position last_write_pos + i.
  *   out_f32: device, fp32 [n_q][H][d].
- * Q is rotated at its positions and quantised to e4m3 per (token, head) row,
- * inside the attention kernel (one launch per call).
+ * Q is rotated at its positions and quantised to e4m3 per (token, head) row.
  * O = softmax(Q K^T / sqrt(d)) V over the valid slots, non-causal, every scale
  * applied per slot.  n_q must equal the latest write's n_tokens (0 is a no-op).
  * Errors: EINVAL, ESTATE (no write yet, n_q mismatch), ECUDA. */
@@ -205,17 +203,15 @@ int kvring_snapshot(const kvring_t* ring, int32_t layer, uint8_t* host_k, uint8_
                     float* host_kamax, float* host_vamax, int32_t* host_pos,
                     int32_t* host_chunk, void* cuda_stream);
 
-/* Synchronous copy of the queries the latest attention call prepared (tests,
- * debug): the e4m3 codes of Q rotated at its positions, quantised per (token,
- * head) row with that row's own amax ([ai.info] "Latenza dei turni...": FP8
- * attention; the query side is quantised the same way as the cache).  The
- * attention kernel keeps them only while kvring_debug_keep_q has switched keeping
- * on (it then also writes them out to the ring's scratch).
+/* Synchronous copy of the latest attention call's prepared queries (tests, debug):
+ * the e4m3 codes of Q rotated at its positions, quantised per (token, head) row
+ * with that row's own amax ([ai.info] "Latenza dei turni...": FP8 attention; the
+ * query side is quantised the same way as the cache).
  *   host_q8:    uint8 [H][n_q][d] codes (may be NULL)
  *   host_qamax: fp32  [H][n_q] row amax, the largest |q| of the rotated row (may be NULL)
  * n_q is the latest kvring_attend's n_q.  Enqueues the copies on cuda_stream and
  * synchronises it.  Errors: EINVAL (NULL ring, host-only ring), ESTATE (no
- * attention call with keeping on), ECUDA. */
+ * attention call yet), ECUDA. */
 int kvring_snapshot_q(const kvring_t* ring, uint8_t* host_q8, float* host_qamax, void* cuda_stream);
 
 /* Synchronise cuda_stream and read the ring's device error word, which kernels set
@@ -238,12 +234,6 @@ int kvring_launch_count(const kvring_t* ring, uint64_t* out);
  * copies in flight, frees its tensor memory and returns.  Errors: EINVAL. */
 int kvring_debug_fault(kvring_t* ring, int32_t skip_tile, int64_t timeout_ns);
 
-/* Testing aid for kvring_snapshot_q: on != 0 makes every later kvring_attend also
- * write the e4m3 query rows and row amax it prepares to the ring's scratch
- * (1.5 MB per call at 757 queries x 16 heads x 128); 0 stops it.  Errors: EINVAL
- * (NULL or host-only ring). */
-int kvring_debug_keep_q(kvring_t* ring, int32_t on);
-
 /* Attention over a caller-held cache that allocates nothing.
  *
  * The pages have no counterpart to this call; it exists for callers that may
@@ -265,7 +255,7 @@ int kvring_debug_keep_q(kvring_t* ring, int32_t on);
  * Slots [0, count) are attended; slots_padded is a multiple of 128 and the K
  * and V codes of slots [count, slots_padded) must be finite (zero will do): they
  * get weight exactly 0, but 0 times a NaN code is not 0.  k8, vt8, kamax,
- * vamax, rope, q and out are 16-byte aligned.
+ * vamax, q and out are 16-byte aligned.
  * err_word: 4 ints, zero before the call.  If a bounded device wait runs out the
  * kernel sets it to KVRING_ETIMEOUT (then kernel, wait site, block), but only
  * while word 0 is still zero: the call does not clear it, so it keeps the first
@@ -273,14 +263,16 @@ int kvring_debug_keep_q(kvring_t* ring, int32_t on);
  * library's own word is used, cleared on the stream at the start of every call,
  * and time-outs go unreported.
  *
- * It allocates nothing and keeps nothing between calls: the queries are
- * prepared inside the attention kernel.  The only memory of the library's own it
- * touches is a fixed 16-byte error word used when err_word is NULL, which every
- * GPU loading the library holds until the process exits.  The first call on a
- * device looks up that word's device address and sets the kernel's attributes
- * (once per device); make that first call before any stream capture.  Uses a
- * single KV split, so for few heads it fills fewer SMs than kvring_attend.
- * Asynchronous on cuda_stream.  Errors (message in
+ * Its only scratch is a fixed array inside the library (the e4m3 Q rows and
+ * their amax): 16,384 rows of (head, query padded to 256), i.e. 2.06 MB that
+ * every GPU loading the library holds until the process exits.  Larger calls
+ * are rejected with KVRING_EINVAL.  The first call on a device looks up that
+ * array's device address (once per device); make that first call before any
+ * stream capture.  Every call shares the array and leaves its last contents
+ * there; each call rewrites all of it that it reads, but calls that overlap on
+ * the GPU (other streams, other threads) race and must be serialised by the
+ * caller.  Uses a single KV split, so for few heads it fills fewer SMs than
+ * kvring_attend.  Asynchronous on cuda_stream.  Errors (message in
  * kvring_last_error(NULL)): EINVAL, ENODEV, ECUDA. */
 int kvring_attend_noalloc(const void* k8, const void* vt8, const float* kamax, const float* vamax,
                           const float* rope, int64_t rope_rows, int64_t q_pos0, const void* q_bf16, int32_t n_q,

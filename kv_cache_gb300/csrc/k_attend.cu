@@ -1,5 +1,4 @@
-// K3 + K4: Q preparation fused into the FP8 attention over the ring, with the
-// KV-split merge.
+// K3 (Q prep) and K4 (FP8 attention over the ring, with the KV-split merge).
 //
 // The pages have every attention call read a cache of 5,788 slots of which 757
 // are new, 240 calls per step (wechild.cn news item on Runway's real-time
@@ -10,13 +9,8 @@
 // dei turni e altre configurazioni GPU").
 //
 // K4 is one CTA of 16 warps per (head, pair of 128-row query tiles, KV split):
-//  * Q is prepared in the kernel (K3): every warp but the TMA producer rotates
-//    the CTA's bf16 query rows at their positions (the latest chunk's), gives
-//    each row one e4m3 scale from its amax, and writes the codes into the query
-//    tiles in shared memory in the layout a 128-byte (d = 128) or 64-byte
-//    (d = 64) swizzled TMA copy would give.  K tiles [128 slots][d], V tiles
-//    [d][128 slots] (e4m3) and the tile's K/V chunk amax rows arrive by TMA into
-//    shared memory, 3 stages.
+//  * Q (e4m3, from K3), K tiles [128 slots][d], V tiles [d][128 slots] (e4m3) and
+//    the tile's K/V chunk amax rows arrive by TMA into shared memory, 3 stages.
 //  * S = Q K^T runs on tcgen05 (kind::f8f6f4, M = 128, N = 64 per half tile)
 //    into tensor memory, two S buffers per query tile.
 //  * Thread i of a softmax warp group owns query row i (tensor-memory lane i):
@@ -45,6 +39,74 @@
 
 
 namespace kvring_impl {
+
+// ============================================================== K3: Q prep
+// Rotate Q at the latest chunk's positions, quantise each (token, head) row to
+// e4m3 with its own amax, write [H][Tstride][d] codes + [H][Tstride] amax.
+// Rows T..Tpad-1 are written as zeros.
+__global__ void __launch_bounds__(128) qprep_kernel(const __grid_constant__ QPrepParams p) {
+    // This grid may have started before the one ahead of it finished, so it
+    // waits for it before reading anything.  Only then may the attention grid
+    // that follows start: that grid loads its first K/V tiles before its own
+    // wait, so the ring must be final (the write ahead of this grid complete)
+    // by the time any of its blocks exists.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int d = p.d;
+    const int tpr = d / 8;                       // threads per row, 8 elements each
+    const int rows_per_block = 128 / tpr;
+    const int lrow = threadIdx.x / tpr;
+    const int c = threadIdx.x % tpr;
+    const int row = blockIdx.x * rows_per_block + lrow;   // over H * Tpad
+    const bool in_range = row < p.H * p.Tpad;
+    const int h = in_range ? row / p.Tpad : 0;
+    const int t = in_range ? row % p.Tpad : 0;
+    const bool real = in_range && t < p.T;
+    float y[8];
+    float amax = 0.f;
+    if (real) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t)t * p.H + h) * d + c * 8));
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        const float2* tab = p.rope + (size_t)(p.pos0 + t) * (d / 2) + c * 4;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 cs = __ldg(tab + e);
+            rope_pair(bf16_lo(ws[e]), bf16_hi(ws[e]), cs.x, cs.y, y[2 * e], y[2 * e + 1]);
+            amax = fmaxf(amax, fmaxf(fabsf(y[2 * e]), fabsf(y[2 * e + 1])));
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = 0.f;
+    }
+    // amax over the tpr lanes of this row (contiguous lanes of one warp)
+    for (int off = tpr / 2; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float inv = inv_of(amax);
+    uint32_t lo = e4m3x2(__fmul_rn(y[0], inv), __fmul_rn(y[1], inv)) | (e4m3x2(__fmul_rn(y[2], inv), __fmul_rn(y[3], inv)) << 16);
+    uint32_t hi = e4m3x2(__fmul_rn(y[4], inv), __fmul_rn(y[5], inv)) | (e4m3x2(__fmul_rn(y[6], inv), __fmul_rn(y[7], inv)) << 16);
+    if (in_range) {
+        *reinterpret_cast<uint2*>(p.q8 + ((size_t)h * p.Tstride + t) * d + c * 8) = make_uint2(lo, hi);
+        if (c == 0) p.qamax[(size_t)h * p.Tstride + t] = amax;
+    }
+}
+
+// Launched with programmatic stream serialisation (its launch overlaps the tail
+// of the grid before it; it waits for that grid before reading anything).
+cudaError_t launch_qprep(const QPrepParams& p, cudaStream_t s) {
+    const int rows_per_block = 128 / (p.d / 8);
+    const int rows = p.H * p.Tpad;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)((rows + rows_per_block - 1) / rows_per_block), 1, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, qprep_kernel, p);
+}
+
+
 
 // ============================================================== K4: attention
 // One CTA of 16 warps per (head, pair of 128-row query tiles, KV split):
@@ -84,14 +146,13 @@ struct AttendSmem {
     static constexpr int offBar = offAm + kStages * kAm;
     static constexpr int kBars = 33;
     static constexpr int offMisc = offBar + kBars * 8;
-    static constexpr int offQa = offMisc + 64;    // row amax of the two query tiles [256]
-    static constexpr int kBytes = offQa + 256 * 4;
+    static constexpr int kBytes = offMisc + 64;
     static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
 // mbarrier slots ([q][b]: per query tile q and S buffer b, in that order)
 enum : int {
-    kBQ = 0,        // query tiles prepared (one arrival after the prep warps' barrier)
+    kBQ = 0,        // query tiles landed (TMA)
     kBKVF = 1,      // [3] stage full: K, V and the amax rows (TMA)
     kBKVE = 4,      // [3] stage free: one arrival per converter warp and per softmax warp (end of its tile)
     kBSF = 7,       // [2][2] S_q half b computed (commit)
@@ -108,7 +169,6 @@ enum : int { kWaitQ = 1, kWaitKVFull = 2, kWaitKVEmpty = 3, kWaitS = 4, kWaitP =
              kWaitV16Empty = 8, kWaitMerge = 9 };
 constexpr int kAttendThreads = 512;
 constexpr int kMaxSplits = 4;   // KV splits per (head, query pair); the merge holds them all in registers
-constexpr int kPrepItemsPerRound = 9;   // Q prep: 480 threads x 9 items cover two d = 128 tiles in one round
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -405,85 +465,6 @@ __device__ __noinline__ float p_general(uint32_t tsrc, uint32_t tdst, const Grou
     return l;
 }
 
-// Q preparation (K3) of the CTA's query tiles, by every warp but the TMA
-// producer (480 threads) right after the grid dependency: item (row, piece) is
-// 8 elements (4 RoPE pairs) of one query row, the NP = D / 8 items of a row in
-// adjacent lanes of one warp.  Each item is rotated at the row's position
-// q_pos0 + qrow (the latest chunk's), the row amax is taken over the rotated
-// values across those lanes, and the item is quantised with 448 / amax (e4m3,
-// round to nearest even, saturating) into row r of its query tile -- in the
-// layout a TMA copy with 128-byte (D = 128) or 64-byte (D = 64) swizzling would
-// give: 16-byte chunk c of row r at r * D + 16 (c ^ (r % 8)), resp.
-// 16 (c ^ ((r / 2) % 4)).  Rows at or past T are zeros (amax 0).  The nrows
-// rows of the tiles (row rr = 128 q + r) are prepared; the row amax goes to
-// qa[rr]; with keep and keep_q8 set, rows below T are also written unswizzled to
-// keep_q8 / keep_qamax.  kPrepItemsPerRound items per thread have their loads in
-// flight at a time; the RoPE entries of the first round are fetched before the
-// grid dependency (griddepcontrol.wait, which every caller needs before it
-// reads q), the rest after it.
-template <int D>
-__device__ __forceinline__ void prep_q_tiles(const AttendParams& p, int h, int pair, int nrows, int pt, uint8_t* sQ,
-                                             float* qa, bool keep) {
-    constexpr int NP = D / 8;
-    constexpr int kPrepThreads = kAttendThreads - 32;
-    constexpr int kPrepItems = kPrepItemsPerRound;
-    const int items = nrows * NP;
-    const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
-    for (int base = 0; base < items; base += kPrepThreads * kPrepItems) {
-        uint4 x[kPrepItems];
-        float4 t0[kPrepItems], t1[kPrepItems];
-#pragma unroll
-        for (int k = 0; k < kPrepItems; ++k) {
-            const int idx = base + pt + k * kPrepThreads;
-            const int rr = idx / NP, c = idx % NP;          // rr: row of the CTA's query tiles
-            const int qrow = 2 * pair * 128 + rr;
-            const bool real = idx < items && qrow < p.T;
-            const float4* tab = reinterpret_cast<const float4*>(p.rope + (size_t)(p.q_pos0 + (real ? qrow : 0)) * (D / 2));
-            t0[k] = real ? __ldg(tab + 2 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
-            t1[k] = real ? __ldg(tab + 2 * c + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        if (base == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
-#pragma unroll
-        for (int k = 0; k < kPrepItems; ++k) {
-            const int idx = base + pt + k * kPrepThreads;
-            const int rr = idx / NP, c = idx % NP;
-            const int qrow = 2 * pair * 128 + rr;
-            const bool real = idx < items && qrow < p.T;
-            x[k] = real ? __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t)qrow * p.H + h) * D) + c) : zero4;
-        }
-#pragma unroll
-        for (int k = 0; k < kPrepItems; ++k) {
-            const int idx = base + pt + k * kPrepThreads;
-            const int rr = idx / NP, c = idx % NP;
-            const int q = rr / 128, r = rr % 128;
-            const int qrow = 2 * pair * 128 + rr;
-            float y[8];
-            rope_pair(bf16_lo(x[k].x), bf16_hi(x[k].x), t0[k].x, t0[k].y, y[0], y[1]);
-            rope_pair(bf16_lo(x[k].y), bf16_hi(x[k].y), t0[k].z, t0[k].w, y[2], y[3]);
-            rope_pair(bf16_lo(x[k].z), bf16_hi(x[k].z), t1[k].x, t1[k].y, y[4], y[5]);
-            rope_pair(bf16_lo(x[k].w), bf16_hi(x[k].w), t1[k].z, t1[k].w, y[6], y[7]);
-            float m = 0.f;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) m = fmaxf(m, fmaxf(fabsf(y[2 * e]), fabsf(y[2 * e + 1])));
-#pragma unroll
-            for (int off = NP / 2; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-            if (idx >= items) continue;
-            const float inv = inv_of(m);
-            const uint2 v = make_uint2(e4m3x2(__fmul_rn(y[0], inv), __fmul_rn(y[1], inv)) |
-                                           (e4m3x2(__fmul_rn(y[2], inv), __fmul_rn(y[3], inv)) << 16),
-                                       e4m3x2(__fmul_rn(y[4], inv), __fmul_rn(y[5], inv)) |
-                                           (e4m3x2(__fmul_rn(y[6], inv), __fmul_rn(y[7], inv)) << 16));
-            const int swz = D == 128 ? (r & 7) : ((r >> 1) & 3);
-            *reinterpret_cast<uint2*>(sQ + q * 128 * D + r * D + 16 * ((c >> 1) ^ swz) + 8 * (c & 1)) = v;
-            if (c == 0) qa[rr] = m;
-            if (keep && p.keep_q8 != nullptr && qrow < p.T) {
-                *reinterpret_cast<uint2*>(p.keep_q8 + ((size_t)h * p.Tstride + qrow) * D + 8 * c) = v;
-                if (c == 0) p.keep_qamax[(size_t)h * p.Tstride + qrow] = m;
-            }
-        }
-    }
-}
-
 template <int D>
 __global__ void __launch_bounds__(kAttendThreads, 1)
 attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ AttendMaps maps) {
@@ -538,30 +519,18 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
     tc_fence_after();
     const uint32_t tmem = *sTmem;
     const int nh = 2 * nt;   // half tiles of 64 slots in one pass over the split
-    float* sQa = reinterpret_cast<float*>(smem + L::offQa);
-
-    // Q prep, by every warp but the producer, which goes straight on to its
-    // loads.  The RoPE entries of the first items are fetched before the grid
-    // dependency (nothing writes the table after the ring is created); q only
-    // after it, since the grid before this one (the write of the ring, or
-    // whatever produced q) has to finish first.  The MMA reads the query tiles
-    // through the async proxy.
-    if (warp != 12) {
-        prep_q_tiles<D>(p, h, pair, 128 * nq, warp < 12 ? tid : tid - 32, sQ, sQa, split == 0);
-        fence_proxy_async_smem();
-        asm volatile("bar.sync 1, %0;" ::"n"(kAttendThreads - 32) : "memory");
-        if (tid == 0) mbar_arrive(&bars[kBQ]);
-    }
 
     // softmax state (warps 0-7), kept for the epilogue
     const int q = warp >> 2;
     const int wq = warp & 3;
     const int row = tid & 127;
+    const int qrow = (2 * pair + q) * 128 + row;
     float M = -INFINITY, l_run = 0.f;
     // producer state (warp 12, lane 0)
     int issued[NST];
 #pragma unroll
     for (int st = 0; st < NST; ++st) issued[st] = 0;
+    bool q_issued = false;
 
     // Register split.  The launch gives each of the 16 warps 128 registers per
     // thread, and every SM sub-partition (warps w, w+4, w+8, w+12) holds two
@@ -590,7 +559,8 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t tS = tmem + 128 * q + lane_off;
         const uint32_t tO = tmem + 256 + 128 * q + lane_off;
-        const float a = scale_of(sQa[q * 128 + row]) * p.log2e_rsqrt_d;
+        asm volatile("griddepcontrol.wait;" ::: "memory");   // Q prep has finished
+        const float a = scale_of(__ldg(p.qamax + (size_t)h * p.Tstride + qrow)) * p.log2e_rsqrt_d;
         float gk[4], gl[4], gi[4];
         bool uni[2];
         int kinds = 0;   // 8 bits per group of the current tile: its kind (0 = one range)
@@ -796,12 +766,22 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
         // The split's tiles twice: K (and the amax rows) for the first pass, then K,
         // V and the amax rows for the second.
         if (lane == 0) {
+            prefetch_tmap(&maps.q8);
             prefetch_tmap(&maps.k8);
             prefetch_tmap(&maps.vt8);
         }
-        // the grid before this one may be the write of the ring
-        asm volatile("griddepcontrol.wait;" ::: "memory");
         for (int ld = 0; ld < 2 * nt; ++ld) {
+            if (ld == (nt < NST ? nt : NST)) {
+                // the query tiles, once the first stages are on their way and Q prep
+                // (the grid before this one) has finished; the stages above could
+                // be issued earlier because this grid starts only after Q prep has
+                // waited for the grid before it (the write of the ring)
+                asm volatile("griddepcontrol.wait;" ::: "memory");
+                mbar_expect_tx_warp(&bars[kBQ], (uint32_t)(nq * L::kQ));
+                tma_load_3d_warp(sQ, &maps.q8, &bars[kBQ], 0, (2 * pair) * 128, h);
+                if (nq == 2) tma_load_3d_warp(sQ + L::kQ, &maps.q8, &bars[kBQ], 0, (2 * pair + 1) * 128, h);
+                q_issued = true;
+            }
             const int st = ld % NST;
             if (ld >= NST && !warp_wait(&bars[kBKVE + st], (uint32_t)(((ld / NST) - 1) & 1), sAbort, p, kWaitKVEmpty))
                 break;
@@ -904,6 +884,7 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
             __syncwarp();
         }
         if (warp == 12 && lane == 0) {
+            if (q_issued) mbar_wait(&bars[kBQ], 0, p.timeout_ns);
             for (int st = 0; st < NST; ++st)
                 if (issued[st] > 0) mbar_wait(&bars[kBKVF + st], (uint32_t)((issued[st] - 1) & 1), p.timeout_ns);
         }
@@ -1130,24 +1111,17 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
     }
 }
 
-cudaError_t attend_setup() {
-    cudaError_t e = cudaFuncSetAttribute(attend_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)AttendSmem<128>::kAlloc);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(attend_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)AttendSmem<64>::kAlloc);
-    return e;
-}
-
-// Launched with programmatic stream serialisation: its CTAs may start (allocate
-// tensor memory, set up barriers) while the grid before it is still running;
-// every thread that reads global memory waits for that grid first
-// (griddepcontrol.wait).  attend_setup() must have run on the device
-// (kvring_create and the allocation-free entry point see to it).
+// Launched with programmatic stream serialisation: its CTAs may start while the
+// Q prep grid before it is still running; they wait for it (griddepcontrol.wait)
+// before reading Q.  Their first K/V loads come before that wait: Q prep lets
+// this grid start only after its own wait, so whatever wrote the ring before Q
+// prep has finished by then.
 cudaError_t launch_attend(const AttendParams& p, const AttendMaps& maps, cudaStream_t s) {
     const int grid = p.H * p.npairs * p.splits;
     const int smem = p.d == 128 ? (int)AttendSmem<128>::kAlloc : (int)AttendSmem<64>::kAlloc;
     void (*kern)(AttendParams, AttendMaps) = p.d == 128 ? attend_kernel<128> : attend_kernel<64>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(kAttendThreads, 1, 1);

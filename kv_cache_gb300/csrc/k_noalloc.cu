@@ -1,6 +1,6 @@
 // kvring_attend_noalloc: the attention call over a cache the caller holds,
-// using no device memory beyond what the caller passes in (and, when the caller
-// passes no error word, one fixed 16-byte word that lives in this file).
+// using no device memory beyond what the caller passes in and one fixed
+// scratch array that lives in this file.
 //
 // Who needs it: callers whose device memory is all handed out up front by
 // their own arena or pool and who may not call cudaMalloc/cudaFree (or any
@@ -9,10 +9,12 @@
 // FP8 cache in it itself.  kvring_create allocates the rings and its scratch;
 // this entry point allocates nothing.
 //
-// The attention kernel prepares the queries itself (rotation, per-row scale,
-// e4m3) into shared memory, so no intermediate goes through global memory.  The
-// call runs the attention with a single KV split, so no split partials or
-// counters are needed either.
+// The only intermediate the attention needs here is the e4m3 copy of Q (and
+// each row's amax), written by the Q-prep kernel and read by the attention
+// kernel through TMA.  It lives in g_noalloc_scratch below, a file-scope
+// __device__ array of fixed size: every GPU that loads this library holds it
+// (2.06 MB) until the process exits.  The call runs the attention with a single
+// KV split, so no split partials or counters are needed.
 #include <cudaTypedefs.h>
 
 #include <cmath>
@@ -23,36 +25,42 @@
 
 namespace kvring_impl {
 
-// The library's own error word, for calls that pass none: 4 ints.
-static __device__ __align__(16) int g_noalloc_err[4];
+// Scratch capacity in (head, padded query row) pairs: 16,384 rows, e.g. 16 heads
+// x 1,024 queries or 64 heads x 256 queries.  Query rows are padded to a
+// multiple of 256 (pairs of 128-row tiles).
+constexpr int kNoAllocMaxRows = 16384;
+constexpr size_t kNoAllocQBytes = (size_t)kNoAllocMaxRows * 128;           // e4m3 Q rows, d <= 128
+constexpr size_t kNoAllocAmaxOff = kNoAllocQBytes;                         // float per row
+constexpr size_t kNoAllocErrOff = kNoAllocAmaxOff + kNoAllocMaxRows * 4;   // spare error word (4 ints)
+constexpr size_t kNoAllocBytes = kNoAllocErrOff + 64;
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocBytes];
 
 namespace {
 
 constexpr int kMaxDevices = 64;
-std::mutex g_setup_mu;
-int* g_err_dev[kMaxDevices] = {};   // device address of g_noalloc_err, per device
+std::mutex g_scratch_mu;
+uint8_t* g_scratch_dev[kMaxDevices] = {};   // device address of g_noalloc_scratch, per device
 
 int noalloc_fail(int code, const std::string& msg) {
     set_thread_error("kvring_attend_noalloc: " + msg);
     return code;
 }
 
-// Device address of the error word on the current device, and the attention
-// kernel's attributes there -- both once per device.  The host-side symbol
-// g_noalloc_err is only a stand-in and must never be handed to a kernel; the
-// address comes from cudaGetSymbolAddress with that device current.
-int device_setup(int dev, int** out) {
-    std::lock_guard<std::mutex> lock(g_setup_mu);
-    if (!g_err_dev[dev]) {
+// Device address of the scratch array on the current device.  The host-side
+// symbol g_noalloc_scratch is only a stand-in and must never be handed to a
+// kernel; the address comes from cudaGetSymbolAddress, once per device, with
+// that device current.
+int scratch_address(int dev, uint8_t** out) {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_dev[dev]) {
         void* ptr = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_err);
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
         if (e != cudaSuccess || !ptr)
             return noalloc_fail(KVRING_ECUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
-        e = attend_setup();
-        if (e != cudaSuccess) return noalloc_fail(KVRING_ECUDA, std::string("kernel attributes: ") + cudaGetErrorString(e));
-        g_err_dev[dev] = static_cast<int*>(ptr);
+        g_scratch_dev[dev] = static_cast<uint8_t*>(ptr);
     }
-    *out = g_err_dev[dev];
+    *out = g_scratch_dev[dev];
     return KVRING_OK;
 }
 
@@ -76,14 +84,18 @@ extern "C" int kvring_attend_noalloc(const void* k8, const void* vt8, const floa
         return noalloc_fail(KVRING_EINVAL, "slots_padded must be a positive multiple of 128");
     if (count < 1 || count > slots_padded) return noalloc_fail(KVRING_EINVAL, "count out of range [1, slots_padded]");
     if (n_q < 0 || q_pos0 < 0) return noalloc_fail(KVRING_EINVAL, "n_q and q_pos0 must be >= 0");
-    // the queries read rope rows q_pos0 .. q_pos0 + n_q - 1
+    // Q prep reads rope rows q_pos0 .. q_pos0 + n_q - 1
     if (rope_rows < 1 || q_pos0 > rope_rows - (int64_t)n_q)
         return noalloc_fail(KVRING_EINVAL, "rope has " + std::to_string(rope_rows) + " rows; the queries need rows up to " +
                                                std::to_string(q_pos0 + n_q - 1));
     const int64_t tstride = ((int64_t)n_q + 255) / 256 * 256;
+    if ((int64_t)num_heads * tstride > kNoAllocMaxRows)
+        return noalloc_fail(KVRING_EINVAL, "num_heads x n_q (padded to 256) = " + std::to_string(num_heads * tstride) +
+                                               " exceeds the fixed scratch of " + std::to_string(kNoAllocMaxRows) +
+                                               " rows; use kvring_attend or split the heads");
     if (!aligned(k8, 16) || !aligned(vt8, 16) || !aligned(q_bf16, 16) || !aligned(out_f32, 16) ||
-        !aligned(kamax, 16) || !aligned(vamax, 16) || !aligned(rope, 16) || (err_word && !aligned(err_word, 4)))
-        return noalloc_fail(KVRING_EINVAL, "k8, vt8, kamax, vamax, rope, q and out must be 16-byte aligned");
+        !aligned(kamax, 16) || !aligned(vamax, 16) || !aligned(rope, 8) || (err_word && !aligned(err_word, 4)))
+        return noalloc_fail(KVRING_EINVAL, "k8, vt8, kamax, vamax, q and out must be 16-byte aligned (rope 8)");
 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -93,13 +105,15 @@ extern "C" int kvring_attend_noalloc(const void* k8, const void* vt8, const floa
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     if (major * 10 + minor != 103) return noalloc_fail(KVRING_ENODEV, "this library is built for sm_103a");
-    int* own_err = nullptr;
-    int rc = device_setup(dev, &own_err);
+    uint8_t* scratch = nullptr;
+    int rc = scratch_address(dev, &scratch);
     if (rc) return rc;
 
     const int H = num_heads, d = head_dim;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-    int* err = err_word ? err_word : own_err;
+    uint8_t* q8 = scratch;
+    float* qamax = reinterpret_cast<float*>(scratch + kNoAllocAmaxOff);
+    int* err = err_word ? err_word : reinterpret_cast<int*>(scratch + kNoAllocErrOff);
     // The library's own word (err_word NULL) starts every call at zero, so a
     // time-out of an earlier call never masks one of this call; a caller's word
     // is left as it is (it keeps the first time-out until the caller clears it).
@@ -107,6 +121,20 @@ extern "C" int kvring_attend_noalloc(const void* k8, const void* vt8, const floa
         e = cudaMemsetAsync(err, 0, 4 * sizeof(int), s);
         if (e != cudaSuccess) return noalloc_fail(KVRING_ECUDA, std::string("clearing the error word: ") + cudaGetErrorString(e));
     }
+
+    // Q prep writes every row of the Q scratch it uses (pad rows as zeros), so
+    // nothing left by an earlier call is read.
+    QPrepParams qp{};
+    qp.q = static_cast<const uint16_t*>(q_bf16);
+    qp.q8 = q8;
+    qp.qamax = qamax;
+    qp.rope = reinterpret_cast<const float2*>(rope);
+    qp.pos0 = q_pos0;
+    qp.T = n_q;
+    qp.Tpad = (n_q + 127) / 128 * 128;
+    qp.H = H;
+    qp.d = d;
+    qp.Tstride = (int)tstride;
 
     AttendMaps maps{};
     const CUtensorMapSwizzle swz_d = d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
@@ -116,18 +144,18 @@ extern "C" int kvring_attend_noalloc(const void* k8, const void* vt8, const floa
     const cuuint64_t vdims[3] = {(cuuint64_t)slots_padded, (cuuint64_t)d, (cuuint64_t)H};
     const cuuint64_t vstr[2] = {(cuuint64_t)slots_padded, (cuuint64_t)slots_padded * d};
     const cuuint32_t vbox[3] = {128, (cuuint32_t)d, 1};
+    const cuuint64_t qdims[3] = {(cuuint64_t)d, (cuuint64_t)tstride, (cuuint64_t)H};
+    const cuuint64_t qstr[2] = {(cuuint64_t)d, (cuuint64_t)tstride * d};
+    const cuuint32_t qbox[3] = {(cuuint32_t)d, 128, 1};
     if ((rc = encode_u8_map(&maps.k8, const_cast<void*>(k8), kdims, kstr, kbox, swz_d)) ||
-        (rc = encode_u8_map(&maps.vt8, const_cast<void*>(vt8), vdims, vstr, vbox, CU_TENSOR_MAP_SWIZZLE_128B)))
+        (rc = encode_u8_map(&maps.vt8, const_cast<void*>(vt8), vdims, vstr, vbox, CU_TENSOR_MAP_SWIZZLE_128B)) ||
+        (rc = encode_u8_map(&maps.q8, q8, qdims, qstr, qbox, swz_d)))
         return noalloc_fail(rc, "tensor map encoding failed");
 
     AttendParams ap{};
     ap.kamax = kamax;
     ap.vamax = vamax;
-    ap.q = static_cast<const uint16_t*>(q_bf16);
-    ap.rope = reinterpret_cast<const float2*>(rope);
-    ap.q_pos0 = q_pos0;
-    ap.keep_q8 = nullptr;
-    ap.keep_qamax = nullptr;
+    ap.qamax = qamax;
     ap.out = out_f32;
     ap.part_o = nullptr;       // one KV split: the kernel writes O straight to out
     ap.part_ml = nullptr;
@@ -150,7 +178,8 @@ extern "C" int kvring_attend_noalloc(const void* k8, const void* vt8, const floa
     ap.coop = 0;
     ap.cluster = 0;
 
-    e = launch_attend(ap, maps, s);
+    e = launch_qprep(qp, s);
+    if (e == cudaSuccess) e = launch_attend(ap, maps, s);
     if (e != cudaSuccess) return noalloc_fail(KVRING_ECUDA, std::string("kernel launch: ") + cudaGetErrorString(e));
     return KVRING_OK;
 }

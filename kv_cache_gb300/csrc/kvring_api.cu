@@ -69,8 +69,7 @@ struct kvring {
     // testing aid
     uint64_t launches = 0;
     int debug_skip_tile = -1;
-    int keep_q = 0;             // testing aid: attention calls keep their prepared Q rows in q8 / qamax
-    int last_q_rows = 0;        // query rows kept by the latest attention call (for kvring_snapshot_q)
+    int last_q_rows = 0;        // query rows of the latest attention call (for kvring_snapshot_q)
     long long debug_timeout_ns = 0;
     std::string error;
 };
@@ -382,7 +381,7 @@ int kvring_create(const kvring_config* cfg_in, kvring_t** out) {
         e = cudaMemcpy(r->rope, tab.data(), rope_bytes, cudaMemcpyHostToDevice);
         if (e != cudaSuccess) { free_device(r); delete r; return fail(nullptr, KVRING_ECUDA, std::string("cudaMemcpy: ") + cudaGetErrorString(e)); }
     }
-    // TMA tensor maps over the rings
+    // TMA tensor maps over the rings and the Q scratch
     {
         const CUtensorMapSwizzle swz_d = d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
         const cuuint64_t kdims[3] = {(cuuint64_t)d, (cuuint64_t)r->Rpad, (cuuint64_t)(L * H)};
@@ -391,10 +390,13 @@ int kvring_create(const kvring_config* cfg_in, kvring_t** out) {
         const cuuint64_t vdims[3] = {(cuuint64_t)r->Rpad, (cuuint64_t)d, (cuuint64_t)(L * H)};
         const cuuint64_t vstr[2] = {(cuuint64_t)r->Rpad, (cuuint64_t)(r->Rpad * d)};
         const cuuint32_t vbox[3] = {128, (cuuint32_t)d, 1};
+        const cuuint64_t qdims[3] = {(cuuint64_t)d, (cuuint64_t)r->Tstride, (cuuint64_t)H};
+        const cuuint64_t qstr[2] = {(cuuint64_t)d, (cuuint64_t)(r->Tstride * d)};
+        const cuuint32_t qbox[3] = {(cuuint32_t)d, 128, 1};
         if ((rc = make_map(nullptr, &r->maps.k8, r->k8, kdims, kstr, kbox, swz_d)) ||
             (rc = make_map(nullptr, &r->maps.vt8, r->vt8, vdims, vstr, vbox, CU_TENSOR_MAP_SWIZZLE_128B)) ||
-            ((cudaSuccess != write_setup() || cudaSuccess != attend_setup()) &&
-             (rc = fail(nullptr, KVRING_ECUDA, "kernel attributes"))) ||
+            (rc = make_map(nullptr, &r->maps.q8, r->q8, qdims, qstr, qbox, swz_d)) ||
+            (cudaSuccess != write_setup() && (rc = fail(nullptr, KVRING_ECUDA, "write kernel attributes"))) ||
             ((rc = write_rope_map(&r->rope_map, r->rope, cfg.max_position, (int)d)) &&
              (rc = fail(nullptr, rc, "tensor map of the RoPE table")))) {
             free_device(r);
@@ -514,16 +516,26 @@ int kvring_attend(kvring_t* r, int32_t layer, const void* q, int32_t n_q, float*
     const int d = c.head_dim, H = c.num_heads;
     const int Tpad = (int)round_up(n_q, 128);
 
-    if (reinterpret_cast<uintptr_t>(q) & 15) return fail(r, KVRING_EINVAL, "q must be 16-byte aligned");
+    QPrepParams qp{};
+    qp.q = static_cast<const uint16_t*>(q);
+    qp.q8 = r->q8;
+    qp.qamax = r->qamax;
+    qp.rope = r->rope;
+    qp.pos0 = L.last_pos;
+    qp.T = n_q;
+    qp.Tpad = Tpad;
+    qp.H = H;
+    qp.d = d;
+    qp.Tstride = (int)r->Tstride;
+    cudaError_t e = launch_qprep(qp, s);
+    if (e != cudaSuccess) return cuda_fail(r, e, "q-prep kernel launch");
+    r->launches += 1;
+
     AttendParams ap{};
     const size_t lh = (size_t)layer * H;
     ap.kamax = r->kamax + lh * r->Rpad;
     ap.vamax = r->vamax + lh * r->Rpad;
-    ap.q = static_cast<const uint16_t*>(q);
-    ap.rope = r->rope;
-    ap.q_pos0 = L.last_pos;
-    ap.keep_q8 = r->keep_q ? r->q8 : nullptr;
-    ap.keep_qamax = r->keep_q ? r->qamax : nullptr;
+    ap.qamax = r->qamax;
     ap.out = out;
     ap.part_o = r->part_o;
     ap.part_ml = r->part_ml;
@@ -554,10 +566,10 @@ int kvring_attend(kvring_t* r, int32_t layer, const void* q, int32_t n_q, float*
     ap.coop = (!ap.cluster && ap.splits > 1 && units * ap.splits <= r->num_sms) ? 1 : 0;
     r->debug_skip_tile = -1;
     r->debug_timeout_ns = 0;
-    const cudaError_t e = launch_attend(ap, r->maps, s);
+    e = launch_attend(ap, r->maps, s);
     if (e != cudaSuccess) return cuda_fail(r, e, "attention kernel launch");
     r->launches += 1;
-    r->last_q_rows = r->keep_q ? n_q : 0;
+    r->last_q_rows = n_q;
     return KVRING_OK;
 }
 
@@ -687,8 +699,7 @@ int kvring_snapshot_q(const kvring_t* rc, uint8_t* hq, float* hqamax, void* stre
     kvring_t* r = const_cast<kvring_t*>(rc);
     if (!r) return KVRING_EINVAL;
     if (r->host_only) return fail(r, KVRING_EINVAL, "no device data on a host-only ring");
-    if (r->last_q_rows <= 0)
-        return fail(r, KVRING_ESTATE, "no attention call since kvring_debug_keep_q switched keeping on");
+    if (r->last_q_rows <= 0) return fail(r, KVRING_ESTATE, "no attention call yet");
     if (!hq && !hqamax) return KVRING_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t H = r->cfg.num_heads, d = r->cfg.head_dim, n = (size_t)r->last_q_rows, ts = (size_t)r->Tstride;
@@ -711,7 +722,7 @@ int kvring_check_device(kvring_t* r, void* stream) {
     if (e == cudaSuccess) e = cudaMemcpy(w, r->err, sizeof(w), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(r, e, "reading the device error word");
     if (w[0] == 0) return KVRING_OK;
-    static const char* sites[] = {"?", "the query tiles", "K/V stage full", "K/V stage free", "S", "P", "O", "fp16 V full",
+    static const char* sites[] = {"?", "Q tiles", "K/V stage full", "K/V stage free", "S", "P", "O", "fp16 V full",
                                   "fp16 V free", "the other KV splits"};
     static const char* write_sites[] = {"?", "the chunk's rows", "the chunk amax from the cluster"};
     if (w[1] == kKernelWrite) {
@@ -747,14 +758,6 @@ int kvring_debug_fault(kvring_t* r, int32_t skip_tile, int64_t timeout_ns) {
     if (skip_tile < -1 || timeout_ns < 0) return fail(r, KVRING_EINVAL, "skip_tile >= -1 and timeout_ns >= 0 required");
     r->debug_skip_tile = skip_tile;
     r->debug_timeout_ns = timeout_ns;
-    return KVRING_OK;
-}
-
-int kvring_debug_keep_q(kvring_t* r, int32_t on) {
-    if (!r) return KVRING_EINVAL;
-    if (r->host_only) return fail(r, KVRING_EINVAL, "no device data on a host-only ring");
-    r->keep_q = on ? 1 : 0;
-    if (!on) r->last_q_rows = 0;
     return KVRING_OK;
 }
 

@@ -98,15 +98,23 @@ struct RebaseParams {
 };
 cudaError_t launch_rebase(const RebaseParams& p, int num_sms, cudaStream_t s);
 
+// ---------------------------------------------------------------- Q prep (K3)
+struct QPrepParams {
+    const uint16_t* q;        // bf16 [T][H][d]
+    uint8_t* q8;              // [H][Tpad][d]
+    float* qamax;             // [H][Tpad]
+    const float2* rope;
+    int64_t pos0;
+    int T, Tpad, H, d;
+    int Tstride;              // row stride of q8 in rows (= Tpad_max)
+};
+cudaError_t launch_qprep(const QPrepParams& p, cudaStream_t s);
+
 // ---------------------------------------------------------------- attention (K4)
 struct AttendParams {
     const float* kamax;       // this layer [H][Rpad]
     const float* vamax;       // this layer [H][Rpad]
-    const uint16_t* q;        // bf16 queries [T][H][d], 16-byte aligned (prepared in the kernel)
-    const float2* rope;       // RoPE table [positions][d/2] (cos, sin)
-    int64_t q_pos0;           // position of query 0
-    uint8_t* keep_q8;         // testing aid: the prepared e4m3 rows [H][Tstride][d] (NULL: not kept)
-    float* keep_qamax;        // and their amax [H][Tstride]
+    const float* qamax;       // [H][Tstride]
     float* out;               // fp32 [T][H][d]
     float* part_o;            // fp32 [splits][H][Tstride][d]   (splits > 1)
     float* part_ml;           // fp32 [splits][H][Tstride][2]   (splits > 1)
@@ -127,10 +135,10 @@ struct AttendParams {
                               // through distributed shared memory (no partials in global memory)
 };
 struct AttendMaps {
+    CUtensorMap q8;           // 3-D {d, Tstride, H}
     CUtensorMap k8;           // 3-D {d, Rpad, L*H}
     CUtensorMap vt8;          // 3-D {Rpad, d, L*H}
 };
-cudaError_t attend_setup();   // function attributes, once per device
 cudaError_t launch_attend(const AttendParams& p, const AttendMaps& maps, cudaStream_t s);
 // How many clusters of `splits` attention CTAs (head dim d) the device holds at once (0 on error).
 int attend_max_clusters(int d, int splits);

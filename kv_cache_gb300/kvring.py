@@ -91,7 +91,6 @@ _SIGNATURES = {
     "kvring_check_device": (ctypes.c_int, [_P, _P]),
     "kvring_last_error": (ctypes.c_char_p, [_P]),
     "kvring_debug_fault": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int64]),
-    "kvring_debug_keep_q": (ctypes.c_int, [_P, ctypes.c_int32]),
     "kvring_launch_count": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint64)]),
     "kvring_attend_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int64, ctypes.c_int64, _P, ctypes.c_int32,
                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P,
@@ -238,10 +237,6 @@ def kvring_debug_fault(ring, skip_tile: int, timeout_ns: int) -> None:
     _check(load().kvring_debug_fault(ring, skip_tile, timeout_ns), ring)
 
 
-def kvring_debug_keep_q(ring, on: bool) -> None:
-    _check(load().kvring_debug_keep_q(ring, 1 if on else 0), ring)
-
-
 def noalloc_arg_error(k8, vt8, kamax, vamax, rope, q_pos0: int, q, out, count: int, err=None, device=None):
     """The first problem with kvring_attend_noalloc's arguments, or None.
 
@@ -302,8 +297,8 @@ def kvring_attend_noalloc(k8, vt8, kamax, vamax, rope, q_pos0: int, q, out, coun
     float32 [H, slots_padded], rope float32 [rows, d/2, 2] with rows >= q_pos0 + n_q,
     q bf16 [n_q, H, d], out float32 [n_q, H, d], err int32 [>= 4] (zero before the
     call; it keeps the first time-out) or None -- all CUDA tensors the caller owns,
-    on the current device (include/kvring.h has the layouts).  Bad arguments raise
-    ValueError before anything is launched.
+    on the current device (include/kvring.h has the layouts and the fixed scratch
+    limit).  Bad arguments raise ValueError before anything is launched.
     """
     msg = noalloc_arg_error(k8, vt8, kamax, vamax, rope, q_pos0, q, out, count, err)
     if msg is not None:
@@ -382,13 +377,8 @@ class KVRing:
     def snapshot(self, layer: int, stream=None, cache: bool = True) -> dict:
         return kvring_snapshot(self.handle, layer, self.H, self.R, self.d, stream, cache)
 
-    def debug_keep_q(self, on: bool = True) -> None:
-        """Make later attention calls keep the queries they prepare, for snapshot_q."""
-        kvring_debug_keep_q(self.handle, on)
-
     def snapshot_q(self, stream=None) -> dict:
-        """The queries the latest attention call prepared (e4m3 codes and row amax);
-        needs debug_keep_q() before that call."""
+        """The latest attention call's prepared queries (e4m3 codes and row amax)."""
         return kvring_snapshot_q(self.handle, self._last_nq, self.H, self.d, stream)
 
     def check_device(self, stream=None) -> int:

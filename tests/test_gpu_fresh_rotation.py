@@ -16,9 +16,7 @@ first reset (before step 42's write) and 31,794 at every later one.
   by the step of the fresh pair's larger element, are printed.
 
 Q preparation (RoPE at the latest chunk's positions, one e4m3 scale per
-(token, head) row), which runs inside the attention kernel, is compared code for
-code with the oracle's: with keeping switched on, the kernel also writes out the
-rows it prepared.
+(token, head) row) is compared code for code with the oracle's.
 """
 import numpy as np
 import pytest
@@ -98,7 +96,6 @@ def test_qprep_codes_match_oracle(R, T, H, d, writes):
     """Q rotated at the latest chunk's positions and quantised per (token, head) row:
     codes and row amax bit-exact with the oracle, before and after a reset."""
     ring = kv.KVRing(1, H, d, R, T, max_position=R + 44 * T)
-    ring.debug_keep_q(True)   # the attention kernel also writes out the rows it prepares
     for w in range(writes):
         if w == writes - 1:
             ring.rebase()

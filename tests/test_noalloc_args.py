@@ -2,7 +2,7 @@
 
 Every bad argument must be refused before anything is launched: by the binding
 (dtypes, shapes, devices, the error word) and, for what raw pointers still
-carry (the RoPE table's row count, alignment), by the
+carry (the RoPE table's row count, the scratch limit, alignment), by the
 library itself, which returns KVRING_EINVAL before its first CUDA call.
 """
 import ctypes
@@ -63,11 +63,10 @@ def test_binding_raises_before_the_library_is_called():
         kv.kvring_attend_noalloc(**{k: v for k, v in _args(count=0).items()})
 
 
-def _raw_call(lib, rope_rows, q_pos0_, n_q_, heads=H, slots=Rp, count=100, align=256, rope_align=256):
+def _raw_call(lib, rope_rows, q_pos0_, n_q_, heads=H, slots=Rp, count=100, align=256):
     p = ctypes.c_void_p(1 << 20)                 # never dereferenced: the checks come first
     odd = ctypes.c_void_p((1 << 20) + 8) if align != 256 else p
-    rope = ctypes.c_void_p((1 << 20) + 8) if rope_align != 256 else p
-    return lib.kvring_attend_noalloc(p, p, p, p, rope, rope_rows, q_pos0_, odd, n_q_, heads, d, slots, count,
+    return lib.kvring_attend_noalloc(p, p, p, p, p, rope_rows, q_pos0_, odd, n_q_, heads, d, slots, count,
                                      p, None, None)
 
 
@@ -77,9 +76,9 @@ def test_library_refuses_before_any_cuda_call():
     assert rc == kv.KVRING_EINVAL and "rope has" in kv.kvring_last_error(None)
     rc = _raw_call(lib, rope_rows=10, q_pos0_=2 ** 40, n_q_=n_q)
     assert rc == kv.KVRING_EINVAL and "rope has" in kv.kvring_last_error(None)
+    rc = _raw_call(lib, rope_rows=10 ** 6, q_pos0_=0, n_q_=300, heads=64)        # 64 x 512 rows > 16,384
+    assert rc == kv.KVRING_EINVAL and "scratch" in kv.kvring_last_error(None)
     rc = _raw_call(lib, rope_rows=10 ** 6, q_pos0_=0, n_q_=n_q, align=8)         # q not 16-byte aligned
-    assert rc == kv.KVRING_EINVAL and "aligned" in kv.kvring_last_error(None)
-    rc = _raw_call(lib, rope_rows=10 ** 6, q_pos0_=0, n_q_=n_q, rope_align=8)    # the table read as float4
     assert rc == kv.KVRING_EINVAL and "aligned" in kv.kvring_last_error(None)
     rc = _raw_call(lib, rope_rows=10 ** 6, q_pos0_=0, n_q_=n_q, count=0)
     assert rc == kv.KVRING_EINVAL

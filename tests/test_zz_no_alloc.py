@@ -2,14 +2,14 @@
 
 kvring_attend_noalloc is for callers that may not allocate device memory because
 their own arena owns all of it: they hold the FP8 cache themselves and the call
-prepares the queries inside the attention kernel, keeping nothing between calls.
-Here a ring is filled through the normal API (and the same chunks go into the
-CPU oracle), its cache is copied into caller-owned tensors in the documented
-layouts, and two calls in a row of the allocation-free entry point must agree,
-within the attention tolerance of the parity tests, with the oracle's float64
-attention over the same cache and queries, and with kvring_attend.  A large call
-is followed by a much smaller one without an error word.  This file is collected
-last on purpose.
+uses only a fixed scratch array inside the library.  Here a ring is filled
+through the normal API (and the same chunks go into the CPU oracle), its cache
+is copied into caller-owned tensors in the documented layouts, and two calls in
+a row of the allocation-free entry point must agree, within the attention
+tolerance of the parity tests, with the oracle's float64 attention over the
+same cache and queries, and with kvring_attend.  A call that fills the whole
+scratch is followed by a much smaller one without an error word, so the second
+runs on scratch left behind by the first.  This file is collected last on purpose.
 """
 import numpy as np
 import pytest
@@ -86,9 +86,9 @@ def test_noalloc_matches_oracle_and_ring_attention_twice(R, T, H, d, writes):
     ring.close()
 
 
-def test_noalloc_small_call_after_a_large_call_without_error_word():
-    # 32 heads x 512 queries, then 2 heads x 32 queries, both with err=None (the
-    # library's own error word)
+def test_noalloc_small_call_after_a_full_scratch_call_without_error_word():
+    # 32 heads x 512 queries fill the 16,384 scratch rows; then 2 heads x 32 queries
+    # with err=None (the library's own error word) read only rows they wrote
     big_ring, big_o = _filled(1024, 512, 32, 64, 2, 900)
     big_st = big_ring.state(0)
     big_cache = _caller_owned_cache(big_ring, 1024, 32, 64, big_st["next_pos"] + 1)
@@ -100,25 +100,22 @@ def test_noalloc_small_call_after_a_large_call_without_error_word():
     for _ in range(2):
         out_big = _noalloc(big_cache, big_st, to_dev(qb_big), None)
         heads, rows = np.array([0, 13, 31]), np.array([0, 1, 127, 128, 300, 511])
-        assert_attention_close(out_big[np.ix_(rows, heads)], big_o.attend(qf_big, heads=heads, rows=rows), "large call")
+        assert_attention_close(out_big[np.ix_(rows, heads)], big_o.attend(qf_big, heads=heads, rows=rows), "full scratch")
         out_small = _noalloc(small_cache, small_st, to_dev(qb_small), None)
-        assert_attention_close(out_small, small_o.attend(qf_small), "small call after a large one")
+        assert_attention_close(out_small, small_o.attend(qf_small), "small call after a full one")
         assert_attention_close(out_small, small_ring.attend(0, to_dev(qb_small)).cpu().numpy(), "vs kvring_attend")
     big_ring.close()
     small_ring.close()
 
 
-def test_noalloc_64_heads_300_queries():
-    # 64 heads x 300 queries (padded: 64 x 512 query rows), d = 64
-    R, T, H, d = 512, 300, 64, 64
-    ring, o = _filled(R, T, H, d, 2, 990)
-    st = ring.state(0)
-    cache = _caller_owned_cache(ring, R, H, d, st["next_pos"] + 1)
-    qb, qf = chunk_pair("q", 991, T, H, d, True)
-    err = torch.zeros(4, dtype=torch.int32, device="cuda")
-    out = _noalloc(cache, st, to_dev(qb), err)
-    assert int(err[0]) == 0
-    heads, rows = np.array([0, 31, 63]), np.array([0, 1, 127, 128, 255, 256, 299])
-    assert_attention_close(out[np.ix_(rows, heads)], o.attend(qf, heads=heads, rows=rows), "64 heads vs oracle")
-    assert_attention_close(out, ring.attend(0, to_dev(qb)).cpu().numpy(), "64 heads vs kvring_attend")
-    ring.close()
+def test_noalloc_rejects_sizes_beyond_its_scratch():
+    H, d, Rp, n = 64, 128, 256, 300          # 64 heads x 512 padded rows > 16,384
+    k8 = torch.zeros((H, Rp, d), dtype=torch.uint8, device="cuda")
+    vt8 = torch.zeros((H, d, Rp), dtype=torch.uint8, device="cuda")
+    ka = torch.zeros((H, Rp), dtype=torch.float32, device="cuda")
+    rope = torch.zeros((n, d // 2, 2), dtype=torch.float32, device="cuda")
+    q = torch.zeros((n, H, d), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((n, H, d), dtype=torch.float32, device="cuda")
+    with pytest.raises(kv.KVRingError) as e:
+        kv.kvring_attend_noalloc(k8, vt8, ka, ka, rope, 0, q, out, 128)
+    assert e.value.code == kv.KVRING_EINVAL and "scratch" in e.value.message
