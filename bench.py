@@ -356,11 +356,28 @@ def run_gpu(args, cfg, rank, world):
     e1.record(stream)
     torch.cuda.synchronize(device)
     e2e_ms = e0.elapsed_time(e1)
-    ring.close()
     del dev_in, dev_out, host_out, pin
-    return dict(ms=ms, w_ms=w_ms, a_ms=a_ms, r_ms=r_ms, rb_ms=rb_ms, launches=launches, clocks=clocks,
-                w_b2b_ms=w_b2b_ms, w_floor_ms=w_floor_ms, e2e_ms=e2e_ms, e2e_steps=e2e_steps, h2d=h2d // e2e_steps, d2h=d2h // e2e_steps,
-                resets_timed=resets_timed)
+    # five more resets, each after one more chunk per block (untimed) so that every
+    # layer has a delta to turn by, with an event pair around each: the median
+    # beside the one reset inside the breakdown pass
+    rb_more = []
+    for i in range(5):
+        s = step_counter[0] + i
+        for l in range(L):
+            j = synthetic.pool_index(s, l, 4, L)
+            ring.write(l, pool["k"][j], pool["v"][j], stream=stream)
+        b0, b1 = mk(), mk()
+        b0.record(stream)
+        ring.rebase(stream)
+        b1.record(stream)
+        torch.cuda.synchronize(device)
+        rb_more.append(b0.elapsed_time(b1))
+    if ring.check_device(stream) != kv.KVRING_OK:
+        raise RuntimeError("device wait timed out after the extra resets: " + kv.kvring_last_error(ring.handle))
+    ring.close()
+    return dict(ms=ms, w_ms=w_ms, a_ms=a_ms, r_ms=r_ms, rb_ms=rb_ms, rb_more=rb_more, launches=launches,
+                clocks=clocks, w_b2b_ms=w_b2b_ms, w_floor_ms=w_floor_ms, e2e_ms=e2e_ms, e2e_steps=e2e_steps,
+                h2d=h2d // e2e_steps, d2h=d2h // e2e_steps, resets_timed=resets_timed)
 
 
 def run_whole_configs_gpu(torch_device_index=0, reps=20):
@@ -996,6 +1013,9 @@ def main():
             "attention_tflops_step": attend_flop * L * P / (a_avg * L * P * 1e-3) / 1e12,
             "rebase_ms": r["rb_ms"],
             "rebase_gbs": (rebase_bytes / (r["rb_ms"] * 1e-3) / 1e9) if r["rb_ms"] else None,
+            "rebase_ms_median_of_5_more": statistics.median(r["rb_more"]) if r.get("rb_more") else None,
+            "rebase_frac_hbm_median_of_5_more": (rebase_bytes / (statistics.median(r["rb_more"]) * 1e-3) / 1e9
+                                                 / peaks["hbm_gbs"]) if r.get("rb_more") else None,
             "hbm_peak_gbs": peaks["hbm_gbs"], "peaks": peak_src,
         },
         "clocks": r["clocks"],

@@ -74,7 +74,7 @@ def test_gpu_arm_line_has_every_contract_key(monkeypatch, capsys):
     sys.path.insert(0, ROOT)
     import bench
     K = 42
-    fake = dict(ms=15.4 * K, w_ms=[0.0166] * 60, w_b2b_ms=0.008, w_floor_ms=0.003, a_ms=[0.0631] * 240, r_ms=[], rb_ms=0.275, launches=25201,
+    fake = dict(ms=15.4 * K, w_ms=[0.0166] * 60, w_b2b_ms=0.008, w_floor_ms=0.003, rb_more=[0.274, 0.275, 0.274, 0.276, 0.274], a_ms=[0.0631] * 240, r_ms=[], rb_ms=0.275, launches=25201,
                 clocks={"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 4},
                 e2e_ms=16.1 * 12, e2e_steps=12, h2d=1116241920, d2h=1488322560, resets_timed=1)
     monkeypatch.setattr(bench, "run_gpu", lambda args, cfg, rank, world: fake)
