@@ -267,13 +267,15 @@ int kvring_debug_fault(kvring_t* ring, int32_t skip_tile, int64_t timeout_ns);
  * their amax): 16,384 rows of (head, query padded to 256), i.e. 2.06 MB that
  * every GPU loading the library holds until the process exits.  Larger calls
  * are rejected with KVRING_EINVAL.  The first call on a device looks up that
- * array's device address (once per device); make that first call before any
- * stream capture.  Every call shares the array and leaves its last contents
+ * array's device address and how many attention clusters the device holds
+ * (once per device); make that first call before any stream capture.  Every call shares the array and leaves its last contents
  * there; each call rewrites all of it that it reads, but calls that overlap on
  * the GPU (other streams, other threads) race and must be serialised by the
- * caller.  Uses a single KV split, so for few heads it fills fewer SMs than
- * kvring_attend.  Asynchronous on cuda_stream.  Errors (message in
- * kvring_last_error(NULL)): EINVAL, ENODEV, ECUDA. */
+ * caller.  KV splits, when the call has them, merge as thread-block clusters
+ * (no partials in memory), so it splits only where every cluster fits on the
+ * device at once and may fill fewer SMs than kvring_attend.  Asynchronous on
+ * cuda_stream.  Errors (message in kvring_last_error(NULL)): EINVAL, ENODEV,
+ * ECUDA. */
 int kvring_attend_noalloc(const void* k8, const void* vt8, const float* kamax, const float* vamax,
                           const float* rope, int64_t rope_rows, int64_t q_pos0, const void* q_bf16, int32_t n_q,
                           int32_t num_heads, int32_t head_dim, int32_t slots_padded, int32_t count,

@@ -13,10 +13,12 @@
 // each row's amax), written by the Q-prep kernel and read by the attention
 // kernel through TMA.  It lives in g_noalloc_scratch below, a file-scope
 // __device__ array of fixed size: every GPU that loads this library holds it
-// (2.06 MB) until the process exits.  The call runs the attention with a single
-// KV split, so no split partials or counters are needed.
+// (2.06 MB) until the process exits.  KV splits, when the call has them, merge
+// as thread-block clusters through distributed shared memory, so no split
+// partials or counters are needed either.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 #include <string>
@@ -41,23 +43,33 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 uint8_t* g_scratch_dev[kMaxDevices] = {};   // device address of g_noalloc_scratch, per device
+int g_num_sms[kMaxDevices] = {};
+int g_cluster_cap[kMaxDevices][2][5] = {};  // [device][d = 64, 128][splits 2..4]: attention clusters held at once
 
 int noalloc_fail(int code, const std::string& msg) {
     set_thread_error("kvring_attend_noalloc: " + msg);
     return code;
 }
 
-// Device address of the scratch array on the current device.  The host-side
-// symbol g_noalloc_scratch is only a stand-in and must never be handed to a
-// kernel; the address comes from cudaGetSymbolAddress, once per device, with
-// that device current.
+// Device address of the scratch array on the current device, and the device's
+// SM count and attention cluster capacities.  The host-side symbol
+// g_noalloc_scratch is only a stand-in and must never be handed to a kernel; the
+// address comes from cudaGetSymbolAddress, once per device, with that device
+// current.
 int scratch_address(int dev, uint8_t** out) {
     std::lock_guard<std::mutex> lock(g_scratch_mu);
     if (!g_scratch_dev[dev]) {
         void* ptr = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
         if (e != cudaSuccess || !ptr)
             return noalloc_fail(KVRING_ECUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess || sms < 1)
+            return noalloc_fail(KVRING_ECUDA, std::string("multiprocessor count: ") + cudaGetErrorString(e));
+        for (int di = 0; di < 2; ++di)
+            for (int sp = 2; sp <= 4; ++sp) g_cluster_cap[dev][di][sp] = attend_max_clusters(di ? 128 : 64, sp);
+        g_num_sms[dev] = sms;
         g_scratch_dev[dev] = static_cast<uint8_t*>(ptr);
     }
     *out = g_scratch_dev[dev];
@@ -170,13 +182,26 @@ extern "C" int kvring_attend_noalloc(const void* k8, const void* vt8, const floa
     ap.layer = 0;
     ap.npairs = (n_q + 255) / 256;
     ap.ntiles = (count + 127) / 128;
-    ap.splits = 1;
-    ap.tiles_per_split = ap.ntiles;
+    // KV splits: as many as keep every CTA in one wave and every cluster of them
+    // on the device at once (fewest tile-times per CTA; one split otherwise)
+    const int units = H * ap.npairs;
+    int best_se = 1, best_tps = ap.ntiles;
+    long long best_cost = -1;
+    for (int sp = 1; sp <= std::min(4, ap.ntiles); ++sp) {
+        const int tps = (ap.ntiles + sp - 1) / sp;
+        const int se = (ap.ntiles + tps - 1) / tps;
+        if (se > 1 && g_cluster_cap[dev][d == 128 ? 1 : 0][se] < units) continue;
+        const long long waves = ((long long)units * se + g_num_sms[dev] - 1) / g_num_sms[dev];
+        const long long cost = waves * tps;
+        if (best_cost < 0 || cost < best_cost) { best_cost = cost; best_se = se; best_tps = tps; }
+    }
+    ap.splits = best_se;
+    ap.tiles_per_split = best_tps;
     ap.log2e_rsqrt_d = (float)(1.4426950408889634 / std::sqrt((double)d));
     ap.timeout_ns = 2000000000LL;
     ap.skip_tile = -1;
     ap.coop = 0;
-    ap.cluster = 0;
+    ap.cluster = best_se > 1 ? 1 : 0;
 
     e = launch_qprep(qp, s);
     if (e == cudaSuccess) e = launch_attend(ap, maps, s);
