@@ -234,6 +234,16 @@ int kvring_launch_count(const kvring_t* ring, uint64_t* out);
  * copies in flight, frees its tensor memory and returns.  Errors: EINVAL. */
 int kvring_debug_fault(kvring_t* ring, int32_t skip_tile, int64_t timeout_ns);
 
+/* The same for the write kernel: the next kvring_write / kvring_write_ex (on a
+ * ring without KVRING_FLAG_NAIVE_UPKEEP) leaves out the TMA copy of ring group
+ * skip_group's rows (16 slots: skip_group * 16 ..) and gives each device wait
+ * timeout_ns nanoseconds (0 = default of 2 s).  The CTA that waits for those
+ * rows records KVRING_ETIMEOUT (kernel: write), still takes part in its
+ * cluster's exchange, waits (bounded) for its other copies and returns without
+ * storing; the chunk's codes are then unreliable until it is written again.
+ * Errors: EINVAL. */
+int kvring_debug_fault_write(kvring_t* ring, int32_t skip_group, int64_t timeout_ns);
+
 /* Attention over a caller-held cache that allocates nothing.
  *
  * The pages have no counterpart to this call; it exists for callers that may

@@ -216,7 +216,8 @@ __global__ void __launch_bounds__(kWriteThreads) write_cluster_kernel(const __gr
     // grid may start now (it waits for this one the same way)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (tid < ng) tma_load_3d(srow + (size_t)tid * 16 * D, is_v ? &p.vmap : &p.kmap, &bars[0], 0, h, t0);
+    if (tid < ng && local_group(p, gb, tid) != p.skip_group)
+        tma_load_3d(srow + (size_t)tid * 16 * D, is_v ? &p.vmap : &p.kmap, &bars[0], 0, h, t0);
     bool ok = mbar_wait(&bars[0], 0, p.timeout_ns);
     if (!ok) write_timed_out(p, kWaitWriteRows);
     if (__syncthreads_and(ok) == 0) ok = false;
@@ -298,8 +299,10 @@ __global__ void __launch_bounds__(kWriteThreads) write_cluster_kernel(const __gr
         }
     }
     // each CTA exits only after all eight maxima have reached it, so no remote
-    // store arrives later
-    const bool got = mbar_wait(&bars[1], 0, p.timeout_ns);
+    // store arrives later.  A CTA whose rows timed out pushes its value only after
+    // that wait (at most timeout_ns), so this wait is given twice that and 1 ms
+    // more: every value pushed arrives before any CTA gives up here.
+    const bool got = mbar_wait(&bars[1], 0, 2 * p.timeout_ns + 1000000LL);
     if (!got) write_timed_out(p, kWaitWriteAmax);
     if (__syncthreads_and(got && ok) == 0) {
         if (!ok) mbar_wait(&bars[0], 0, p.timeout_ns);   // no box left in flight into this CTA (bounded again)

@@ -69,6 +69,8 @@ struct kvring {
     // testing aid
     uint64_t launches = 0;
     int debug_skip_tile = -1;
+    int debug_skip_group = -1;          // testing aid for the write kernel's waits
+    long long debug_write_timeout_ns = 0;
     int last_q_rows = 0;        // query rows of the latest attention call (for kvring_snapshot_q)
     long long debug_timeout_ns = 0;
     std::string error;
@@ -473,7 +475,10 @@ int kvring_write_ex(kvring_t* r, int32_t layer, const void* k, const void* v, in
         p.amax_blocks = (n + p.amax_tokens_per_block - 1) / p.amax_tokens_per_block;
         p.part = r->wpart;
         p.err = r->err;
-        p.timeout_ns = 2000000000LL;
+        p.timeout_ns = r->debug_write_timeout_ns > 0 ? r->debug_write_timeout_ns : 2000000000LL;
+        p.skip_group = r->debug_skip_group;
+        r->debug_skip_group = -1;
+        r->debug_write_timeout_ns = 0;
         p.ropemap = r->rope_map;
         if (write_input_maps(p) != KVRING_OK) return fail(r, KVRING_ECUDA, "tensor maps of the chunk's K and V");
         cudaError_t e = launch_write(p, static_cast<cudaStream_t>(stream));
@@ -758,6 +763,14 @@ int kvring_debug_fault(kvring_t* r, int32_t skip_tile, int64_t timeout_ns) {
     if (skip_tile < -1 || timeout_ns < 0) return fail(r, KVRING_EINVAL, "skip_tile >= -1 and timeout_ns >= 0 required");
     r->debug_skip_tile = skip_tile;
     r->debug_timeout_ns = timeout_ns;
+    return KVRING_OK;
+}
+
+int kvring_debug_fault_write(kvring_t* r, int32_t skip_group, int64_t timeout_ns) {
+    if (!r) return KVRING_EINVAL;
+    if (skip_group < -1 || timeout_ns < 0) return fail(r, KVRING_EINVAL, "skip_group >= -1 and timeout_ns >= 0 required");
+    r->debug_skip_group = skip_group;
+    r->debug_write_timeout_ns = timeout_ns;
     return KVRING_OK;
 }
 

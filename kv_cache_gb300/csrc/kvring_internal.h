@@ -41,6 +41,7 @@ struct WriteParams {
     float* part;              // per-block amax partials [K|V][amax_blocks][H] (ring scratch)
     int* err;                 // the ring's device error word
     long long timeout_ns;     // bound of each device wait
+    int skip_group;           // testing aid: the rows of this ring group are not loaded (-1 = off)
 };
 cudaError_t write_setup();                                        // function attributes, once per device
 cudaError_t launch_write(const WriteParams& p, cudaStream_t s);   // one launch (clusters)

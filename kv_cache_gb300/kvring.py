@@ -91,6 +91,7 @@ _SIGNATURES = {
     "kvring_check_device": (ctypes.c_int, [_P, _P]),
     "kvring_last_error": (ctypes.c_char_p, [_P]),
     "kvring_debug_fault": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int64]),
+    "kvring_debug_fault_write": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int64]),
     "kvring_launch_count": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint64)]),
     "kvring_attend_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int64, ctypes.c_int64, _P, ctypes.c_int32,
                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P,
@@ -235,6 +236,10 @@ def kvring_launch_count(ring) -> int:
 
 def kvring_debug_fault(ring, skip_tile: int, timeout_ns: int) -> None:
     _check(load().kvring_debug_fault(ring, skip_tile, timeout_ns), ring)
+
+
+def kvring_debug_fault_write(ring, skip_group: int, timeout_ns: int) -> None:
+    _check(load().kvring_debug_fault_write(ring, skip_group, timeout_ns), ring)
 
 
 def noalloc_arg_error(k8, vt8, kamax, vamax, rope, q_pos0: int, q, out, count: int, err=None, device=None):
