@@ -13,7 +13,8 @@ A "step" is one pass of the whole hot path: [rebase when due] + 60 x write +
   its own GPU; no data-path collective), inputs resident in HBM.
 * e2e: the same steps with each step's K, V, Q copied host->device from pinned
   memory and all 240 attention outputs (one buffer per layer and pass) copied
-  back to pinned host memory, inside the timed region.
+  back to pinned host memory, inside the timed region; one copy per kind and
+  step (the chunks laid out contiguously), on a second stream.
 * The timed steps start at a reset step (positions reset before that step's
   writes), so K timed steps hold ceil(K / 42) rebases: at least the reset's
   share of the path, never less.
@@ -293,42 +294,49 @@ def run_gpu(args, cfg, rank, world):
     del g_write, g_floor, wk, wv, floor_out
 
     # ---- end to end: host inputs (pinned) -> device, all attention outputs -> host, every step.
-    # Two buffer sets: a copy stream brings step s + 1's K, V and Q in while step s
-    # computes, and reads step s's 240 outputs back once it has finished (the way a
-    # serving loop overlaps its transfers); every step's copies are inside the
-    # timed region.
+    # Two device buffer sets: a copy stream brings step s + 1's K, V and Q in while
+    # step s computes, and reads step s's 240 outputs back once it has finished
+    # (the way a serving loop overlaps its transfers); every step's copies are
+    # inside the timed region.  Each kind moves as one copy per step (a step's K,
+    # V and Q chunks laid out contiguously in pinned memory, its outputs in one
+    # device buffer), so the host issues 4 copies per step instead of one per
+    # tensor and the loop does not wait on the host.
     e2e_steps = max(1, min(K, args.e2e_steps))
-    pin = {r: [torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).pin_memory() for b in host[r]] for r in host}
+    nk, nq = L * WP, L * P
+    chunk = (T, H, d)
+    host_in = {"k": torch.empty((nk,) + chunk, dtype=torch.bfloat16, pin_memory=True),
+               "v": torch.empty((nk,) + chunk, dtype=torch.bfloat16, pin_memory=True),
+               "q": torch.empty((nq,) + chunk, dtype=torch.bfloat16, pin_memory=True)}
+    for l in range(L):            # one step's inputs, from the pool (the same bytes every step)
+        for p in range(WP):
+            i = synthetic.pool_index(0, l, 4 if p == 0 else p, L)
+            host_in["k"][p * L + l].copy_(torch.from_numpy(host["k"][i].view(np.int16)).view(torch.bfloat16))
+            host_in["v"][p * L + l].copy_(torch.from_numpy(host["v"][i].view(np.int16)).view(torch.bfloat16))
+        for p in range(P):
+            i = synthetic.pool_index(0, l, p, L)
+            host_in["q"][p * L + l].copy_(torch.from_numpy(host["q"][i].view(np.int16)).view(torch.bfloat16))
+    host_out = torch.empty((nq,) + chunk, dtype=torch.float32, pin_memory=True)
     NB = 2
-    dev_in = [{"k": [torch.empty((T, H, d), dtype=torch.bfloat16, device=device) for _ in range(L * WP)],
-               "v": [torch.empty((T, H, d), dtype=torch.bfloat16, device=device) for _ in range(L * WP)],
-               "q": [torch.empty((T, H, d), dtype=torch.bfloat16, device=device) for _ in range(L * P)]}
-              for _ in range(NB)]
-    dev_out = [outs] + [[torch.empty((T, H, d), dtype=torch.float32, device=device) for _ in range(L * P)]
-                        for _ in range(NB - 1)]
-    host_out = [[torch.empty((T, H, d), dtype=torch.float32).pin_memory() for _ in range(L * P)] for _ in range(NB)]
+    dev_in = [{kind: torch.empty_like(host_in[kind], device=device) for kind in host_in} for _ in range(NB)]
+    dev_out = [torch.empty((nq,) + chunk, dtype=torch.float32, device=device) for _ in range(NB)]
+    dev_in_views = [{kind: list(dev_in[b][kind].unbind(0)) for kind in dev_in[b]} for b in range(NB)]
+    dev_out_views = [list(dev_out[b].unbind(0)) for b in range(NB)]
     cs = torch.cuda.Stream(device)
     ev = lambda: torch.cuda.Event()
     in_ready, comp_done, out_read = [ev() for _ in range(NB)], [ev() for _ in range(NB)], [ev() for _ in range(NB)]
     h2d = d2h = 0
     to_reset_step()
-    s0 = step_counter[0]
 
     def issue_inputs(n):
         nonlocal h2d
-        s, b = s0 + n, n % NB
+        b = n % NB
         with torch.cuda.stream(cs):
             if n >= NB:
                 cs.wait_event(comp_done[b])      # the step that last read slot b has finished
-            for l in range(L):
-                for p in range(WP):
-                    i = synthetic.pool_index(s, l, 4 if p == 0 else p, L)
-                    dev_in[b]["k"][p * L + l].copy_(pin["k"][i], non_blocking=True)
-                    dev_in[b]["v"][p * L + l].copy_(pin["v"][i], non_blocking=True)
-                for p in range(P):
-                    dev_in[b]["q"][p * L + l].copy_(pin["q"][synthetic.pool_index(s, l, p, L)], non_blocking=True)
+            for kind in ("k", "v", "q"):
+                dev_in[b][kind].copy_(host_in[kind], non_blocking=True)
             in_ready[b].record(cs)
-        h2d += (2 * L * WP + P * L) * T * H * d * 2
+        h2d += sum(t.numel() * t.element_size() for t in host_in.values())
 
     torch.cuda.synchronize(device)
     e0, e1 = mk(), mk()
@@ -342,21 +350,20 @@ def run_gpu(args, cfg, rank, world):
         stream.wait_event(in_ready[b])
         if n >= NB:
             stream.wait_event(out_read[b])       # step n - 2's outputs are read back
-        one_step(inputs=dev_in[b], out_bufs=dev_out[b])
+        one_step(inputs=dev_in_views[b], out_bufs=dev_out_views[b])
         comp_done[b].record(stream)
         with torch.cuda.stream(cs):
             cs.wait_event(comp_done[b])
-            for i in range(L * P):
-                host_out[b][i].copy_(dev_out[b][i], non_blocking=True)
+            host_out.copy_(dev_out[b], non_blocking=True)
             out_read[b].record(cs)
-        d2h += L * P * T * H * d * 4
+        d2h += host_out.numel() * host_out.element_size()
     fin = ev()
     fin.record(cs)
     stream.wait_event(fin)
     e1.record(stream)
     torch.cuda.synchronize(device)
     e2e_ms = e0.elapsed_time(e1)
-    del dev_in, dev_out, host_out, pin
+    del dev_in, dev_out, dev_in_views, dev_out_views, host_out, host_in
     # five more resets, each after one more chunk per block (untimed) so that every
     # layer has a delta to turn by, with an event pair around each: the median
     # beside the one reset inside the breakdown pass
