@@ -294,10 +294,10 @@ def run_gpu(args, cfg, rank, world):
     del g_write, g_floor, wk, wv, floor_out
 
     # ---- end to end: host inputs (pinned) -> device, all attention outputs -> host, every step.
-    # Two device buffer sets: a copy stream brings step s + 1's K, V and Q in while
-    # step s computes, and reads step s's 240 outputs back once it has finished
-    # (the way a serving loop overlaps its transfers); every step's copies are
-    # inside the timed region.  Each kind moves as one copy per step (a step's K,
+    # Two device buffer sets: one copy stream brings step s + 1's K, V and Q in
+    # while step s computes, another reads step s's 240 outputs back once it has
+    # finished (the way a serving loop overlaps its transfers; the two directions
+    # use separate copy engines); every step's copies are inside the timed region.  Each kind moves as one copy per step (a step's K,
     # V and Q chunks laid out contiguously in pinned memory, its outputs in one
     # device buffer), so the host issues 4 copies per step instead of one per
     # tensor and the loop does not wait on the host.
@@ -321,7 +321,8 @@ def run_gpu(args, cfg, rank, world):
     dev_out = [torch.empty((nq,) + chunk, dtype=torch.float32, device=device) for _ in range(NB)]
     dev_in_views = [{kind: list(dev_in[b][kind].unbind(0)) for kind in dev_in[b]} for b in range(NB)]
     dev_out_views = [list(dev_out[b].unbind(0)) for b in range(NB)]
-    cs = torch.cuda.Stream(device)
+    cs = torch.cuda.Stream(device)          # host -> device
+    cs_out = torch.cuda.Stream(device)      # device -> host: the two directions run at once
     ev = lambda: torch.cuda.Event()
     in_ready, comp_done, out_read = [ev() for _ in range(NB)], [ev() for _ in range(NB)], [ev() for _ in range(NB)]
     h2d = d2h = 0
@@ -352,14 +353,16 @@ def run_gpu(args, cfg, rank, world):
             stream.wait_event(out_read[b])       # step n - 2's outputs are read back
         one_step(inputs=dev_in_views[b], out_bufs=dev_out_views[b])
         comp_done[b].record(stream)
-        with torch.cuda.stream(cs):
-            cs.wait_event(comp_done[b])
+        with torch.cuda.stream(cs_out):
+            cs_out.wait_event(comp_done[b])
             host_out.copy_(dev_out[b], non_blocking=True)
-            out_read[b].record(cs)
+            out_read[b].record(cs_out)
         d2h += host_out.numel() * host_out.element_size()
-    fin = ev()
+    fin, fin_out = ev(), ev()
     fin.record(cs)
+    fin_out.record(cs_out)
     stream.wait_event(fin)
+    stream.wait_event(fin_out)
     e1.record(stream)
     torch.cuda.synchronize(device)
     e2e_ms = e0.elapsed_time(e1)
