@@ -80,6 +80,26 @@ def test_write_long_chunks(R, T, H, d, writes):
     assert ring.check_device() == kv.KVRING_OK
 
 
+def test_write_and_attend_at_the_head_limit():
+    """256 heads (the library's limit): the write's 4,096 CTAs (a cluster of 8 per
+    head and K|V) and the attention's grid, codes bit-exact, attention in tolerance."""
+    R, T, H, d = 160, 48, 256, 64
+    ring = kv.KVRing(1, H, d, R, T, max_position=4096)
+    o = WriteTimeRing(R, H, d)
+    for w in range(5):                       # fills and wraps
+        kb, kf = chunk_pair("k", 500 + w, T, H, d, True)
+        vb, vf = chunk_pair("v", 500 + w, T, H, d, True)
+        ring.write(0, to_dev(kb), to_dev(vb))
+        o.write(kf, vf)
+        fk, fv = _check_cache(ring, 0, o)
+        assert fk == 1.0 and fv == 1.0
+    qb, qf = chunk_pair("q", 505, T, H, d, True)
+    heads = np.array([0, 77, 128, 255])
+    out = ring.attend(0, to_dev(qb)).cpu().numpy()
+    assert_attention_close(out[:, heads], o.attend(qf, heads=heads), "256 heads")
+    assert ring.check_device() == kv.KVRING_OK
+
+
 # (600, 150, 2, 64): as the ring fills, 2, 3, 4 and 3 KV splits, merged as clusters
 @pytest.mark.parametrize("R,T,H,d", [(96, 32, 2, 64), (100, 32, 2, 64), (300, 100, 2, 128), (600, 150, 2, 64)])
 def test_attend_small(R, T, H, d):
