@@ -789,7 +789,7 @@ def oracle_upkeep_sample(cfg):
 # DRAM bytes (read + write) per attend_kernel launch, from the ncu capture summarised
 # in profiles/attend_kernel_production_ring_8_blocks.md; valid only for the attention
 # source it was taken on (sha256 prefix), else reported as null.
-ATTEND_TRAFFIC = {"bytes": 26.79e6, "source_sha256": "efdf3becdebff800",
+ATTEND_TRAFFIC = {"bytes": 26.77e6, "source_sha256": "7f6d94254698a4c2",
                   "shape": {"H": 16, "d": 128, "R": 5788, "T": 757}}
 
 

@@ -1115,13 +1115,14 @@ attend_kernel(const __grid_constant__ AttendParams p, const __grid_constant__ At
 // Q prep grid before it is still running; they wait for it (griddepcontrol.wait)
 // before reading Q.  Their first K/V loads come before that wait: Q prep lets
 // this grid start only after its own wait, so whatever wrote the ring before Q
-// prep has finished by then.
+// prep has finished by then.  The kernel's shared-memory attribute is set once
+// per device by attend_max_clusters (kvring_create asks it for the ring's d, the
+// allocation-free entry point for both), so a launch makes no other CUDA call
+// and can be captured into a graph.
 cudaError_t launch_attend(const AttendParams& p, const AttendMaps& maps, cudaStream_t s) {
     const int grid = p.H * p.npairs * p.splits;
     const int smem = p.d == 128 ? (int)AttendSmem<128>::kAlloc : (int)AttendSmem<64>::kAlloc;
     void (*kern)(AttendParams, AttendMaps) = p.d == 128 ? attend_kernel<128> : attend_kernel<64>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(kAttendThreads, 1, 1);
@@ -1144,6 +1145,8 @@ cudaError_t launch_attend(const AttendParams& p, const AttendMaps& maps, cudaStr
     return cudaLaunchKernelEx(&cfg, kern, p, maps);
 }
 
+// Also sets the kernel's dynamic shared-memory attribute on the current device,
+// which every launch needs.
 int attend_max_clusters(int d, int splits) {
     const int smem = d == 128 ? (int)AttendSmem<128>::kAlloc : (int)AttendSmem<64>::kAlloc;
     void (*kern)(AttendParams, AttendMaps) = d == 128 ? attend_kernel<128> : attend_kernel<64>;
