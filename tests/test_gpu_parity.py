@@ -80,6 +80,25 @@ def test_write_long_chunks(R, T, H, d, writes):
     assert ring.check_device() == kv.KVRING_OK
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_write_whole_ring_chunks_from_mid_group(d):
+    """Chunks as long as the ring (T = R = 2,048) written from a slot inside a
+    16-slot group: the chunk's last tokens land in its first slot's group, before
+    its first token.  Bit-exact with the oracle after each write."""
+    R = T = 2048
+    H = 2
+    ring = kv.KVRing(1, H, d, R, T, max_position=4 * T)
+    o = WriteTimeRing(R, H, d)
+    for w, n in enumerate([5, T, 21, T, T]):
+        kb, kf = chunk_pair("k", 600 + w, T, H, d, True)
+        vb, vf = chunk_pair("v", 600 + w, T, H, d, True)
+        ring.write(0, to_dev(kb[:n]), to_dev(vb[:n]))
+        o.write(kf[:n], vf[:n])
+        fk, fv = _check_cache(ring, 0, o)
+        assert fk == 1.0 and fv == 1.0, f"write {w} ({n} tokens): {fk}, {fv}"
+    assert ring.check_device() == kv.KVRING_OK
+
+
 def test_write_and_attend_at_the_head_limit():
     """256 heads (the library's limit): the write's 4,096 CTAs (a cluster of 8 per
     head and K|V) and the attention's grid, codes bit-exact, attention in tolerance."""
